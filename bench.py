@@ -1,0 +1,467 @@
+#!/usr/bin/env python
+"""Benchmark: MSDA forward + backward at Deformable-DETR encoder scale on GB300.
+
+One step = one forward and one full backward (zero, accumulate, finish) of
+the encoder workload (B=2, Q=S=22223, M=8, D=32, L=4, K=4; synthetic inputs
+drawn by scale_deformable_attention_msda_gb300.workloads), with every input
+resident in HBM. L2 is flushed (a 256 MiB write) between timed steps, outside
+the timed events. Each kernel is bracketed by CUDA events on the launching
+stream, so the step time and every kernel's time come from the device clock.
+
+Printed (rank 0, one JSON line): queries/s for the whole job, ms per step,
+per-kernel times and HBM fractions, the roofline of the dominant kernel, the
+end-to-end number through the public API with host buffers (copies inside the
+timed region), the fp64 CPU oracle timed on the host cores as a baseline, and
+the SM clocks sampled during the run.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--dtype bf16|f32|f16]
+                  [--accum fp32_buffer|native] [--impl ours|reference]
+Under torchrun each rank runs its own replica (weak scaling); the time is the
+maximum over ranks. --impl reference times the fp64 CPU oracle instead.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "MSDA fwd+bwd queries/sec at encoder scale; achieved HBM GB/s vs GB300 peak"
+UNIT = "queries/s"
+FLUSH_BYTES = 256 << 20
+FALLBACK_HBM_GBS = 6800.0
+
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=100)
+    ap.add_argument("--dtype", default="bf16", choices=["bf16", "f32", "f16"])
+    ap.add_argument("--accum", default="fp32_buffer", choices=["fp32_buffer", "native"])
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=50)
+    a = ap.parse_args(argv)
+    if a.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    return a
+
+
+def dist_env():
+    return (int(os.environ.get("RANK", 0)), int(os.environ.get("LOCAL_RANK", 0)),
+            int(os.environ.get("WORLD_SIZE", 1)))
+
+
+# ------------------------------------------------------------ multi-rank
+# Each rank is an independent replica; the only exchange is the timing
+# reduction below (no collective on the data path).
+
+def reduce_max(x: float, device=None) -> float:
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()):
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def reduce_sum(x: float, device=None) -> float:
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()):
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+def barrier(device_index=None):
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized():
+        if device_index is not None and dist.get_backend() == "nccl":
+            dist.barrier(device_ids=[device_index])
+        else:
+            dist.barrier()
+
+
+def job_throughput(units_this_rank: float, seconds_this_rank: float, device=None) -> tuple:
+    """(whole-job units per second, max seconds over ranks, total units)."""
+    total = reduce_sum(units_this_rank, device)
+    slowest = reduce_max(seconds_this_rank, device)
+    return total / slowest, slowest, total
+
+
+# ---------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi samples every 100 ms while the GPU works (read-only)."""
+
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,utilization.gpu,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    REASONS = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+
+    def __init__(self, uuid=None):
+        self.lines = []
+        self.proc = None
+        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+               "-lms", "100"]
+        if uuid:
+            cmd.insert(1, f"--id={uuid}")
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                                         text=True)
+        except OSError:
+            return
+        self.t = threading.Thread(target=self._read, daemon=True)
+        self.t.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.t.join(timeout=2)
+        rows = []
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                rows.append({"sm": float(f[1]), "max": float(f[2]), "util": float(f[4]),
+                             "reasons": [r for r, v in zip(self.REASONS, f[5:9]) if v == "Active"]})
+            except ValueError:
+                continue
+        if not rows:
+            return None
+        busy = [r for r in rows if r["util"] > 0] or rows
+        reasons = sorted({x for r in busy for x in r["reasons"]})
+        return {"sm_mhz": statistics.median(r["sm"] for r in busy),
+                "sm_max_mhz": max(r["max"] for r in rows), "reasons": reasons,
+                "samples": len(busy)}
+
+
+def measured_hbm_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def profiled_traffic(kernel: str):
+    """DRAM bytes per launch of `kernel` from the committed ncu summary, or None.
+
+    profiles/<kernel>_encoder.md carries a line
+    `traffic_bytes_per_launch: N  source_sha256: H`; it counts only while the
+    kernel sources still hash to H."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", f"{kernel}_encoder.md")
+    try:
+        text = open(path).read()
+    except OSError:
+        return None
+    import re
+    m = re.search(r"traffic_bytes_per_launch:\s*(\d+)\s+source_sha256:\s*([0-9a-f]+)", text)
+    if not m:
+        return None
+    return int(m.group(1)) if m.group(2) == kernel_source_hash() else None
+
+
+def kernel_source_hash() -> str:
+    import hashlib
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "scale_deformable_attention_msda_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cu", ".cuh")):
+            h.update(name.encode())
+            h.update(open(os.path.join(csrc, name), "rb").read())
+    return h.hexdigest()[:16]
+
+
+# ---------------------------------------------------------- CPU baseline
+
+def cpu_baseline(p, seconds: float = 10.0, max_reps: int = 20, nthreads: int = 0):
+    """The fp64 oracle, as it stands, on the host cores: forward + backward of
+    the full workload, repeated for about `seconds`."""
+    import numpy as np
+    import oracle
+    oracle.build()
+    f64 = {k: np.ascontiguousarray(p[k], dtype=np.float64)
+           for k in ("value", "loc", "attn", "grad_out")}
+    B, Q = f64["loc"].shape[:2]
+    times = []
+    t_end = time.perf_counter() + seconds
+    while len(times) < max_reps and (len(times) < 2 or time.perf_counter() < t_end):
+        t0 = time.perf_counter()
+        oracle.forward(f64["value"], p["shapes"], p["starts"], f64["loc"], f64["attn"],
+                       nthreads=nthreads)
+        oracle.backward(f64["value"], p["shapes"], p["starts"], f64["loc"], f64["attn"],
+                        f64["grad_out"], nthreads=nthreads)
+        times.append(time.perf_counter() - t0)
+    t = statistics.median(times)
+    return {"value": B * Q / t, "unit": UNIT, "cores": nthreads or (os.cpu_count() or 1),
+            "kind": "oracle",
+            "sample": f"full workload (B={B}, Q={Q}), forward+backward in fp64, "
+                      f"median of {len(times)} repetitions"}
+
+
+# ------------------------------------------------------------- our arm
+
+def run_ours(args):
+    import numpy as np
+    import torch
+    import torch.distributed as dist
+
+    from scale_deformable_attention_msda_gb300 import binding, build, workloads as wl
+
+    rank, local_rank, world = dist_env()
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=dev)
+    if rank == 0 or not os.path.exists(build.LIBRARY):
+        build.build()
+    barrier(local_rank)
+    binding.lib()
+
+    tdt = {"bf16": torch.bfloat16, "f32": torch.float32, "f16": torch.float16}[args.dtype]
+    accum = binding.MSDA_ACC_FP32_BUFFER if args.accum == "fp32_buffer" else binding.MSDA_ACC_NATIVE
+    w = wl.encoder(args.dtype, variant=rank)
+    p = wl.make_inputs(w)
+
+    def up(a):
+        return torch.tensor(a, dtype=torch.float64).to(tdt).to(dev)
+
+    value, loc, attn, gout = up(p["value"]), up(p["loc"]), up(p["attn"]), up(p["grad_out"])
+    shapes = torch.tensor(p["shapes"], device=dev)
+    starts = torch.tensor(p["starts"], device=dev)
+    out = torch.empty((w.B, w.Q, w.M * w.D), dtype=tdt, device=dev)
+    buf = binding.BackwardBuffers(value, loc, attn, accum)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step(ev=None):
+        if ev:
+            ev[0].record(stream)
+        binding.msda_forward(value, shapes, starts, loc, attn, out=out)
+        if ev:
+            ev[1].record(stream)
+        binding.msda_backward_zero(buf, tdt)
+        if ev:
+            ev[2].record(stream)
+        binding.msda_backward_accumulate(value, shapes, starts, loc, attn, gout, buf)
+        if ev:
+            ev[3].record(stream)
+        binding.msda_backward_finish(buf, tdt)
+        if ev:
+            ev[4].record(stream)
+
+    uuid = None
+    try:
+        uuid = str(torch.cuda.get_device_properties(dev).uuid)
+        uuid = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
+    except Exception:
+        uuid = None
+    sampler = ClockSampler(uuid) if rank == 0 else None
+
+    for _ in range(args.warmup):
+        flush.fill_(1)
+        step()
+    torch.cuda.synchronize()
+    barrier(local_rank)
+    torch.cuda.synchronize()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    for i in range(args.steps):
+        flush.fill_(i & 0xff)
+        step(evs[i])
+    torch.cuda.synchronize()
+    barrier(local_rank)
+    torch.cuda.synchronize()
+    clocks = sampler.stop() if sampler else None
+
+    names = ("forward", "zero", "backward", "finish")
+    per = {n: [evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(args.steps)]
+           for j, n in enumerate(names)}
+    step_ms = [evs[i][0].elapsed_time(evs[i][4]) for i in range(args.steps)]
+    total_s = sum(step_ms) / 1e3
+    qps, slowest_s, total_units = job_throughput(w.B * w.Q * args.steps, total_s, dev)
+    ms_per_step = slowest_s * 1e3 / args.steps
+
+    # ---- end to end through the public API, host buffers, copies timed
+    host = {k: torch.tensor(p[k], dtype=torch.float64).to(tdt).pin_memory()
+            for k in ("value", "loc", "attn", "grad_out")}
+    host_out = {"out": torch.empty(out.shape, dtype=tdt).pin_memory(),
+                "gv": torch.empty(value.shape, dtype=tdt).pin_memory(),
+                "gl": torch.empty(loc.shape, dtype=tdt).pin_memory(),
+                "ga": torch.empty(attn.shape, dtype=tdt).pin_memory()}
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = sum(t.numel() * t.element_size() for t in host_out.values())
+    e2e_ms = []
+    for i in range(args.e2e_steps + 3):
+        flush.fill_(i & 0xff)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        value.copy_(host["value"], non_blocking=True)
+        loc.copy_(host["loc"], non_blocking=True)
+        attn.copy_(host["attn"], non_blocking=True)
+        gout.copy_(host["grad_out"], non_blocking=True)
+        binding.msda_forward(value, shapes, starts, loc, attn, out=out)
+        binding.msda_backward(value, shapes, starts, loc, attn, gout, accum=accum,
+                              grad_value=buf.grad_value,
+                              grad_sampling_locations=buf.grad_sampling_locations,
+                              grad_attention_weights=buf.grad_attention_weights,
+                              workspace=buf.workspace)
+        host_out["out"].copy_(out, non_blocking=True)
+        host_out["gv"].copy_(buf.grad_value, non_blocking=True)
+        host_out["gl"].copy_(buf.grad_sampling_locations, non_blocking=True)
+        host_out["ga"].copy_(buf.grad_attention_weights, non_blocking=True)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        if i >= 3:
+            e2e_ms.append(e0.elapsed_time(e1))
+    e2e_qps, _, _ = job_throughput(w.B * w.Q * len(e2e_ms), sum(e2e_ms) / 1e3, dev)
+
+    # ---- roofline of the dominant kernel
+    cb = wl.compulsory_bytes(w)
+    algo = {"forward": cb["forward"], "backward": cb["backward"]}
+    mean = {n: statistics.fmean(v) for n, v in per.items()}
+    dominant = max(("forward", "backward"), key=lambda n: mean[n])
+    peak, peak_kind = measured_hbm_peak()
+    kernel_name = {"forward": "msda_forward_kernel", "backward": "msda_backward_kernel"}
+    achieved = algo[dominant] / (mean[dominant] * 1e-3) / 1e9
+    traffic = profiled_traffic(kernel_name[dominant])
+    roofline = {"bound": "hbm", "kernel": kernel_name[dominant], "achieved": round(achieved, 1),
+                "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
+                "traffic": traffic, "algorithmic_bytes": algo[dominant],
+                "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
+                else "fallback 6.8 TB/s"}
+    kernels = {}
+    for n in names:
+        k = {"ms": round(mean[n], 5), "launches": args.steps}
+        if n in algo:
+            gbs = algo[n] / (mean[n] * 1e-3) / 1e9
+            k.update(algorithmic_bytes=algo[n], gbs=round(gbs, 1), hbm_frac=round(gbs / peak, 4))
+        kernels[n] = k
+    step_bytes = cb["forward"] + cb["backward"]
+
+    result = None
+    if rank == 0:
+        cpu = None
+        if world == 1 and not args.no_cpu_baseline:
+            cpu = cpu_baseline(p)
+        launches_per_step = 4 if (args.dtype != "f32" and accum == binding.MSDA_ACC_FP32_BUFFER) else 3
+        result = {
+            "metric": METRIC, "value": round(qps, 1), "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f32", "data": "synthetic",
+            "config": {"workload": "deformable-detr encoder: B=2, Q=S=22223, M=8, D=32, L=4, K=4, "
+                                   "levels (100,167),(50,84),(25,42),(13,21)",
+                       "storage_dtype": args.dtype, "grad_value_accumulator": args.accum,
+                       "global_batch": w.B * world, "queries_per_step": w.B * w.Q * world,
+                       "parallelism": f"replicas x{world}" if world > 1 else "single gpu",
+                       "l2": "flushed between timed steps (256 MiB write, outside the events)",
+                       "step": "msda_forward + msda_backward (zero, accumulate, finish)"},
+            "step_hbm": {"compulsory_bytes": step_bytes,
+                         "gbs": round(step_bytes / (ms_per_step * 1e-3) / 1e9, 1),
+                         "frac": round(step_bytes / (ms_per_step * 1e-3) / 1e9 / peak, 4)},
+            "kernels": kernels,
+            "roofline": roofline,
+            "cpu_baseline": cpu,
+            "e2e": {"value": round(e2e_qps, 1), "unit": UNIT, "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h, "steps": len(e2e_ms),
+                    "ms_per_step": round(statistics.fmean(e2e_ms), 4)},
+            "gpu_launches": launches_per_step * args.steps,
+            "clocks": clocks,
+            "kernel_source_sha256": kernel_source_hash(),
+        }
+        print(json.dumps(result), flush=True)
+    if world > 1:
+        barrier(local_rank)
+        dist.destroy_process_group()
+    return result
+
+
+# ------------------------------------------------------- reference arm
+
+def run_reference(args):
+    """The fp64 CPU oracle, as it stands, timed on the host cores."""
+    rank, _, world = dist_env()
+    if rank != 0:
+        return None
+    import numpy as np
+    import oracle
+    from scale_deformable_attention_msda_gb300 import workloads as wl
+
+    oracle.build()
+    w = wl.encoder(args.dtype)
+    p = wl.make_inputs(w)
+    f64 = {k: np.ascontiguousarray(p[k], dtype=np.float64) for k in ("value", "loc", "attn", "grad_out")}
+
+    def step(n):
+        oracle.forward(f64["value"], p["shapes"], p["starts"], f64["loc"][:, :n], f64["attn"][:, :n])
+        oracle.backward(f64["value"], p["shapes"], p["starts"], f64["loc"][:, :n],
+                        f64["attn"][:, :n], f64["grad_out"][:, :n])
+
+    # size each step so that warmup + steps take about 90 s in all
+    t0 = time.perf_counter()
+    step(2048)
+    t = time.perf_counter() - t0
+    budget = 90.0 / (args.steps + args.warmup)
+    n = int(min(w.Q, max(256, 2048 * budget / max(t, 1e-6))))
+    for _ in range(args.warmup):
+        step(n)
+    times = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        step(n)
+        times.append(time.perf_counter() - t0)
+    total = sum(times)
+    qps = w.B * n * args.steps / total
+    cores = os.cpu_count() or 1
+    result = {
+        "impl": "reference", "metric": METRIC, "value": round(qps, 1), "unit": UNIT,
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(total * 1e3 / args.steps, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": "deformable-detr encoder: B=2, Q=S=22223, M=8, D=32, L=4, K=4",
+                   "sample_queries_per_batch": n, "storage_dtype": args.dtype},
+        "cpu_baseline": {"value": round(qps, 1), "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": f"first {n} queries of each of the B={w.B} batches per step, "
+                                   "forward+backward in fp64 against the full value tensor"},
+        "e2e": {"value": round(qps, 1), "unit": UNIT, "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(result), flush=True)
+    return result
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

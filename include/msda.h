@@ -1,0 +1,207 @@
+/*
+ * libmsda -- multi-scale deformable attention (MSDA) for GB300 (sm_103a).
+ *
+ * C ABI. Every pointer argument named as a tensor is a DEVICE pointer to a
+ * dense, row-major (C-contiguous) array; the library allocates nothing, frees
+ * nothing and keeps no state between calls. Every call is asynchronous: it
+ * validates its arguments on the host, enqueues its kernels on `stream` (a
+ * cudaStream_t passed as void*; NULL is the legacy default stream) and returns.
+ * A non-OK status means nothing was enqueued, except MSDA_ERR_CUDA, which
+ * reports the error of a launch that the runtime rejected.
+ *
+ * The operator is the bracketed term of Eq. 1 of Deformable DETR as the
+ * msda-triton course, ch. 1 "Deformable attention, from scratch" states it
+ * (sections "The equation, term by term" and "Bilinear interpolation"):
+ *
+ *   out[b,q,m*D+d] = sum_{l<L} sum_{k<K} A[b,q,m,l,k] *
+ *                    bilinear(value[b, level l, m, d], loc[b,q,m,l,k,:])
+ *
+ * with pixel coordinates x = loc_x*W_l - 0.5, y = loc_y*H_l - 0.5 (the
+ * grid_sample align_corners=False convention), the four corners
+ * (y0,x0), (y0,x0+1), (y0+1,x0), (y0+1,x0+1) of x0 = floor(x), y0 = floor(y)
+ * weighted (1-lx)(1-ly), lx(1-ly), (1-lx)ly, lx*ly, and zero for a corner
+ * outside [0,W_l) x [0,H_l). Level l occupies value rows
+ * [level_start_index[l], level_start_index[l] + H_l*W_l), pixel (y, x) at
+ * row level_start_index[l] + y*W_l + x.
+ *
+ * Operands (shapes use B batch, S = sum_l H_l*W_l value rows, Q queries,
+ * M heads, D channels per head, L levels, K points per level):
+ *   value                (B, S, M, D)        float type `dtype`
+ *   spatial_shapes       (L, 2) int64        rows (H_l, W_l)
+ *   level_start_index    (L,)   int64        exclusive prefix sum of H_l*W_l
+ *   sampling_locations   (B, Q, M, L, K, 2)  `dtype`, last dim (x, y), normalised
+ *   attention_weights    (B, Q, M, L, K)     `dtype`, used as given
+ *   out                  (B, Q, M*D)         `dtype`
+ * Sampling locations may be anything, including off the map, infinite or
+ * NaN: a sample none of whose corners is inside the map contributes zero and
+ * receives zero gradient. The integer parts (x0, y0) are the exact floor of
+ * the real number loc*W - 0.5 for the stored loc. value and grad_out must be
+ * finite: a corner outside the map is read from a clamped in-map row with
+ * weight zero, so a non-finite value there would leak into the result.
+ * A level whose table entry is not a non-empty rectangle inside [0, S)
+ * (H_l < 1, W_l < 1, start < 0 or start + H_l*W_l > S) is treated as empty.
+ *
+ * Arithmetic: products and sums in fp32 for every storage dtype; a 16-bit
+ * result is rounded once, to nearest even, when it is stored.
+ */
+#ifndef MSDA_H
+#define MSDA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define MSDA_API __attribute__((visibility("default")))
+#else
+#define MSDA_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Storage type of every float operand of one call. */
+typedef enum {
+    MSDA_F32 = 0,
+    MSDA_BF16 = 1,
+    MSDA_F16 = 2
+} msda_dtype_t;
+
+/* How msda_backward accumulates grad_value for a 16-bit dtype.
+ * NATIVE: vector atomic adds straight into the 16-bit grad_value (each add
+ *   rounds to the 16-bit format, so the result depends on contention).
+ * FP32_BUFFER: atomic adds into a caller-provided fp32 workspace, then one
+ *   rounding pass into grad_value. For MSDA_F32 both modes are the same
+ *   (fp32 atomics into grad_value) and no workspace is needed.
+ * The pages motivate the switch: the Efficient-MSDA summary page, section
+ * "The backward pass is an atomics problem", and the deformops README,
+ * section "Backend selection" (fp32 accumulator vs native half atomics). */
+typedef enum {
+    MSDA_ACC_NATIVE = 0,
+    MSDA_ACC_FP32_BUFFER = 1
+} msda_accum_t;
+
+typedef enum {
+    MSDA_OK = 0,
+    MSDA_ERR_NULL = 1,      /* a required pointer is NULL                      */
+    MSDA_ERR_SHAPE = 2,     /* a dimension is out of the supported range       */
+    MSDA_ERR_DTYPE = 3,     /* unknown dtype or accumulation mode              */
+    MSDA_ERR_ALIGN = 4,     /* a pointer is not aligned as required            */
+    MSDA_ERR_WORKSPACE = 5, /* workspace missing or smaller than required      */
+    MSDA_ERR_CUDA = 6       /* the CUDA runtime rejected a launch              */
+} msda_status_t;
+
+/* Problem sizes. Supported: B >= 0, Q >= 0 (zero is a valid empty call),
+ * S >= 1, M >= 1, 1 <= L <= 16, K >= 1, S*M*D < 2^31, and D a power-of-two
+ * multiple of the 16-byte vector width: D/4 in {1,2,4,...,32} for MSDA_F32,
+ * D/8 in {1,2,4,...,32} for 16-bit dtypes (D = 32 is the detector case). */
+typedef struct {
+    int64_t B, S, Q, M, D, L, K;
+} msda_dims_t;
+
+/* Forward: writes out (B, Q, M*D). The bracketed term of Eq. 1 (see top).
+ * query_order: NULL for linear dispatch, else a device int32 permutation of
+ *   [0, Q) shared by every batch; dispatch slot i computes query
+ *   query_order[i]. The result does not depend on it (Efficient-MSDA page,
+ *   "Two heuristics that do not apply": dispatch order is a scheduling knob).
+ *   A slot whose entry lies outside [0, Q) computes nothing; an array that is
+ *   not a permutation leaves some outputs unwritten.
+ * Alignment: value and out 16 bytes; sampling_locations 2*element size;
+ *   attention_weights element size; spatial_shapes, level_start_index 8.
+ * Errors: MSDA_ERR_NULL, _SHAPE, _DTYPE, _ALIGN before any launch;
+ *   MSDA_ERR_CUDA if the launch is rejected. */
+MSDA_API msda_status_t msda_forward(const void *value, const int64_t *spatial_shapes,
+                           const int64_t *level_start_index,
+                           const void *sampling_locations,
+                           const void *attention_weights,
+                           const int32_t *query_order, void *out,
+                           const msda_dims_t *dims, msda_dtype_t dtype,
+                           void *stream);
+
+/* Bytes of device workspace msda_backward needs: B*S*M*D*4 for a 16-bit
+ * dtype with MSDA_ACC_FP32_BUFFER, else 0. Returns 0 for invalid dims. */
+MSDA_API size_t msda_backward_workspace_bytes(const msda_dims_t *dims,
+                                     msda_dtype_t dtype, msda_accum_t accum);
+
+/* Backward: given grad_out (B, Q, M*D), OVERWRITES
+ *   grad_value               (B, S, M, D)       d loss / d value
+ *   grad_sampling_locations  (B, Q, M, L, K, 2) d loss / d loc
+ *   grad_attention_weights   (B, Q, M, L, K)    d loss / d attention weight
+ * The three gradients the msda-triton course index names for chapter 5
+ * ("The backward kernel"), derived from the forward by the chain rule: with
+ * g = grad_out[b,q,m,:] and s_c = <g, value[corner c]> (0 outside the map),
+ *   grad_attn = sum_c w_c s_c,   grad_value[corner c] += a w_c g,
+ *   grad_loc_x = a W_l ((1-ly)(s_01-s_00) + ly(s_11-s_10)),
+ *   grad_loc_y = a H_l ((1-lx)(s_10-s_00) + lx(s_11-s_01)).
+ * No per-sample intermediate buffer is used (deformops README, "Zero-buffer
+ * kernels"). grad_value is accumulated with atomics, so its rounding order is
+ * not deterministic; the other two gradients are.
+ * workspace: device memory of at least msda_backward_workspace_bytes(...)
+ *   bytes, 16-byte aligned, owned by the caller (may be NULL when 0 bytes
+ *   are needed). Its contents are overwritten.
+ * Alignment: value, grad_out, grad_value 16 bytes; sampling_locations and
+ *   grad_sampling_locations 2*element size; attention weights and their
+ *   gradient element size.
+ * Errors: as msda_forward, plus MSDA_ERR_WORKSPACE. */
+MSDA_API msda_status_t msda_backward(const void *value, const int64_t *spatial_shapes,
+                            const int64_t *level_start_index,
+                            const void *sampling_locations,
+                            const void *attention_weights,
+                            const int32_t *query_order, const void *grad_out,
+                            void *grad_value, void *grad_sampling_locations,
+                            void *grad_attention_weights, void *workspace,
+                            size_t workspace_bytes, msda_accum_t accum,
+                            const msda_dims_t *dims, msda_dtype_t dtype,
+                            void *stream);
+
+/* The same backward in three steps, for callers that sum grad_value over
+ * several calls sharing one value tensor (or that time the kernels apart).
+ * msda_backward(...) is exactly zero + accumulate + finish on one stream.
+ *
+ * msda_backward_zero: zeroes the accumulation target -- the fp32 workspace
+ *   for a 16-bit dtype with MSDA_ACC_FP32_BUFFER, else grad_value.
+ * msda_backward_accumulate: ADDS this call's contribution into that target
+ *   and overwrites grad_sampling_locations and grad_attention_weights.
+ *   Arguments as msda_backward.
+ * msda_backward_finish: rounds the fp32 workspace into grad_value (16-bit
+ *   dtype with MSDA_ACC_FP32_BUFFER); does nothing in the other modes.
+ * Errors: as msda_backward. */
+MSDA_API msda_status_t msda_backward_zero(void *grad_value, void *workspace,
+                                          size_t workspace_bytes, msda_accum_t accum,
+                                          const msda_dims_t *dims, msda_dtype_t dtype,
+                                          void *stream);
+MSDA_API msda_status_t msda_backward_accumulate(
+    const void *value, const int64_t *spatial_shapes, const int64_t *level_start_index,
+    const void *sampling_locations, const void *attention_weights,
+    const int32_t *query_order, const void *grad_out, void *grad_value,
+    void *grad_sampling_locations, void *grad_attention_weights, void *workspace,
+    size_t workspace_bytes, msda_accum_t accum, const msda_dims_t *dims,
+    msda_dtype_t dtype, void *stream);
+MSDA_API msda_status_t msda_backward_finish(const void *workspace, size_t workspace_bytes,
+                                            void *grad_value, msda_accum_t accum,
+                                            const msda_dims_t *dims, msda_dtype_t dtype,
+                                            void *stream);
+
+/* The integer parts every kernel uses, for bit-exact checks (same device
+ * code as the forward and backward kernels). For each sample s (flattened
+ * (b,q,m,l,k)) and corner c in order 00, 01, 10, 11, writes to the device
+ * array corner_rows (B*Q*M*L*K*4 int32) the value row
+ * level_start_index[l] + yy*W_l + xx of a corner inside the map, -1 for a
+ * corner outside it. D of dims is not used. */
+MSDA_API msda_status_t msda_debug_corners(const int64_t *spatial_shapes,
+                                 const int64_t *level_start_index,
+                                 const void *sampling_locations,
+                                 int32_t *corner_rows, const msda_dims_t *dims,
+                                 msda_dtype_t dtype, void *stream);
+
+/* Static description of a status code (never NULL). */
+MSDA_API const char *msda_status_string(msda_status_t status);
+
+/* Library version, major*10000 + minor*100 + patch. */
+MSDA_API int msda_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MSDA_H */

@@ -1,0 +1,340 @@
+// MSDA backward on sm_103a.
+//
+// The three gradients named by the msda-triton course index, chapter 5 ("The
+// backward kernel"), derived from the forward by the chain rule. For a sample
+// with attention weight a, bilinear weights w_c and g = grad_out[b,q,m,:]:
+//   s_c        = <g, value[corner c]>            (0 for a corner off the map)
+//   grad_attn  = sum_c w_c s_c
+//   grad_value[corner c] += a w_c g              (vector atomics, relaxed)
+//   grad_loc_x = a W ((1-ly)(s_01 - s_00) + ly (s_11 - s_10))
+//   grad_loc_y = a H ((1-lx)(s_10 - s_00) + lx (s_11 - s_01))
+//
+// Work split as in the forward: a group of LPG lanes owns one (b,q,m), each
+// lane 16 bytes of its D channels. Per chunk of samples a warp
+//  1. prepares descriptors (lane per sample): corner rows, a*w_c for the
+//     scatter, and keeps lx, ly, a, W, H and the corner mask in registers;
+//  2. gathers (group per sample): four 16-byte corner loads, per-lane partial
+//     dot products with g, vector atomic adds of a*w_c*g into grad_value, and
+//     an xor-butterfly that completes the four dot products across the group;
+//  3. finishes (lane per sample, the lane that prepared it): grad_attn and
+//     grad_loc from the four dot products, one coalesced store each.
+// No per-sample buffer exists outside shared memory (deformops README,
+// "Zero-buffer kernels").
+//
+// Accumulation of grad_value (Efficient-MSDA summary page, "The backward pass
+// is an atomics problem"; deformops README, "Backend selection"): fp32 data
+// uses red.global.add.v4.f32; 16-bit data either adds natively with
+// red.global.add.noftz.v4.{bf16x2,f16x2} (8 channels per instruction) or adds
+// in fp32 into a workspace that a second kernel rounds into grad_value.
+#include "msda_common.cuh"
+
+namespace msda {
+
+__device__ __forceinline__ void red_add_v4_f32(float *p, float a, float b, float c, float d) {
+    asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(a), "f"(b),
+                 "f"(c), "f"(d)
+                 : "memory");
+}
+__device__ __forceinline__ void red_add_v4_bf16x2(void *p, uint4 v) {
+    asm volatile("red.global.add.noftz.v4.bf16x2 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x),
+                 "r"(v.y), "r"(v.z), "r"(v.w)
+                 : "memory");
+}
+__device__ __forceinline__ void red_add_v4_f16x2(void *p, uint4 v) {
+    asm volatile("red.global.add.noftz.v4.f16x2 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x),
+                 "r"(v.y), "r"(v.z), "r"(v.w)
+                 : "memory");
+}
+
+// grad_value[p .. p+VEC) += w * g for one lane's VEC channels.
+template <typename T, bool F32ACC> struct Scatter;
+template <> struct Scatter<float, true> {
+    using Acc = float;
+    static __device__ __forceinline__ void add(float *p, float w, const float *g) {
+        red_add_v4_f32(p, w * g[0], w * g[1], w * g[2], w * g[3]);
+    }
+};
+template <typename T> struct Scatter<T, true> {  // 16-bit data, fp32 workspace
+    using Acc = float;
+    static __device__ __forceinline__ void add(float *p, float w, const float *g) {
+        red_add_v4_f32(p, w * g[0], w * g[1], w * g[2], w * g[3]);
+        red_add_v4_f32(p + 4, w * g[4], w * g[5], w * g[6], w * g[7]);
+    }
+};
+template <> struct Scatter<__nv_bfloat16, false> {
+    using Acc = __nv_bfloat16;
+    static __device__ __forceinline__ void add(__nv_bfloat16 *p, float w, const float *g) {
+        float t[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) t[i] = w * g[i];
+        red_add_v4_bf16x2(p, pack16<__nv_bfloat16>(t));
+    }
+};
+template <> struct Scatter<__half, false> {
+    using Acc = __half;
+    static __device__ __forceinline__ void add(__half *p, float w, const float *g) {
+        float t[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) t[i] = w * g[i];
+        red_add_v4_f16x2(p, pack16<__half>(t));
+    }
+};
+
+template <typename T> __device__ __forceinline__ void store_xy(T *p, float x, float y);
+template <> __device__ __forceinline__ void store_xy<float>(float *p, float x, float y) {
+    *reinterpret_cast<float2 *>(p) = make_float2(x, y);
+}
+template <> __device__ __forceinline__ void store_xy<__nv_bfloat16>(__nv_bfloat16 *p, float x, float y) {
+    *reinterpret_cast<__nv_bfloat162 *>(p) = __floats2bfloat162_rn(x, y);
+}
+template <> __device__ __forceinline__ void store_xy<__half>(__half *p, float x, float y) {
+    *reinterpret_cast<__half2 *>(p) = __floats2half2_rn(x, y);
+}
+
+template <typename T, int LPG, bool F32ACC>
+__global__ void __launch_bounds__(kThreads)
+msda_backward_kernel(const Params p) {
+    constexpr int VEC = Vec16<T>::N;
+    constexpr int GPW = 32 / LPG;
+    constexpr int SPW = 64;
+    constexpr int CH = SPW / GPW;
+    constexpr int NP = SPW / 32;             // samples each lane prepares per chunk
+    constexpr int U = CH < 2 ? CH : 2;
+    using S = Scatter<T, F32ACC>;
+    using Acc = typename S::Acc;
+
+    __shared__ LevelTable lt;
+    __shared__ float4 s_w[kWarpsPerBlock][SPW];
+    __shared__ int4 s_o[kWarpsPerBlock][SPW];
+    __shared__ float4 s_dot[kWarpsPerBlock][SPW];
+
+    load_level_table(lt, p);
+    __syncthreads();
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int g = lane / LPG, r = lane % LPG;
+    const int64_t t0 = ((int64_t)blockIdx.x * kWarpsPerBlock + warp) * GPW;
+    if (t0 >= p.triples) return;
+
+    const int64_t t = t0 + g;
+    const bool active = t < p.triples;
+    const Triple tr = triple_of(active ? t : t0, p);
+    const bool valid_q = active && tr.q >= 0 && tr.q < p.Q;
+    const int64_t vrow = ((int64_t)tr.b * p.S * p.M + tr.m) * p.D + r * VEC;
+    const T *vbase = reinterpret_cast<const T *>(p.value) + vrow;
+    Acc *gvbase = reinterpret_cast<Acc *>(p.grad_value) + vrow;
+
+    // this lane's slice of grad_out (zero for a group with nothing to do)
+    float go[VEC];
+    if (valid_q) {
+        unpack16<T>(go, ldg16(reinterpret_cast<const T *>(p.grad_out) + tr.bqm * p.D + r * VEC));
+    } else {
+#pragma unroll
+        for (int i = 0; i < VEC; ++i) go[i] = 0.0f;
+    }
+
+    int64_t prep_bqm[NP];
+    bool prep_ok[NP];
+#pragma unroll
+    for (int i = 0; i < NP; ++i) {
+        const int s = lane + 32 * i;
+        const int64_t ts = t0 + s / CH;
+        prep_ok[i] = ts < p.triples;
+        const Triple trs = triple_of(prep_ok[i] ? ts : t0, p);
+        prep_ok[i] = prep_ok[i] && trs.q >= 0 && trs.q < p.Q;
+        prep_bqm[i] = trs.bqm;
+    }
+
+    const T *loc = reinterpret_cast<const T *>(p.loc);
+    const T *attn = reinterpret_cast<const T *>(p.attn);
+    T *gloc = reinterpret_cast<T *>(p.grad_loc);
+    T *gattn = reinterpret_cast<T *>(p.grad_attn);
+
+    for (int base = 0; base < p.LK; base += CH) {
+        // ---- phase 1: descriptors, and the finishing state of each sample
+        float f_lx[NP], f_ly[NP], f_a[NP], f_W[NP], f_H[NP];
+        unsigned f_mask[NP];
+#pragma unroll
+        for (int i = 0; i < NP; ++i) {
+            const int s = lane + 32 * i;
+            const int gs = s / CH, j = s % CH;
+            const int idx = base + j;
+            float4 w = make_float4(0.f, 0.f, 0.f, 0.f);
+            int4 o = make_int4(0, 0, 0, 0);
+            f_lx[i] = f_ly[i] = f_a[i] = f_W[i] = f_H[i] = 0.0f;
+            f_mask[i] = 0u;
+            if (prep_ok[i] && idx < p.LK) {
+                const int64_t e = prep_bqm[i] * p.LK + idx;
+                const float2 xy = load_xy<T>(loc + 2 * e);
+                const float a = load_scalar<T>(attn + e);
+                const int l = level_of(idx, p.inv_K);
+                SampleGeom sg;
+                sample_geometry(sg, xy.x, xy.y, lt, l);
+                const unsigned m = (sg.vx0 && sg.vy0 ? 1u : 0u) | (sg.vx1 && sg.vy0 ? 2u : 0u) |
+                                   (sg.vx0 && sg.vy1 ? 4u : 0u) | (sg.vx1 && sg.vy1 ? 8u : 0u);
+                const float hx = 1.0f - sg.lx, hy = 1.0f - sg.ly;
+                const float ahy = a * hy, aly = a * sg.ly;
+                w.x = (m & 1u) ? ahy * hx : 0.0f;
+                w.y = (m & 2u) ? ahy * sg.lx : 0.0f;
+                w.z = (m & 4u) ? aly * hx : 0.0f;
+                w.w = (m & 8u) ? aly * sg.lx : 0.0f;
+                o = make_int4(sg.row[0] * p.MD, sg.row[1] * p.MD, sg.row[2] * p.MD,
+                              sg.row[3] * p.MD);
+                f_lx[i] = sg.lx;
+                f_ly[i] = sg.ly;
+                f_a[i] = a;
+                f_W[i] = lt.Wf[l];
+                f_H[i] = lt.Hf[l];
+                f_mask[i] = m;
+            }
+            s_w[warp][j * GPW + gs] = w;
+            s_o[warp][j * GPW + gs] = o;
+        }
+        __syncwarp();
+
+        // ---- phase 2: gather, dot products, scatter
+        const int n = min(CH, p.LK - base);
+        for (int j = 0; j < n; j += U) {
+            float4 w[U];
+            int4 o[U];
+            uint4 v[U][4];
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                w[u] = s_w[warp][(j + u) * GPW + g];
+                o[u] = s_o[warp][(j + u) * GPW + g];
+                v[u][0] = ldg16(vbase + o[u].x);
+                v[u][1] = ldg16(vbase + o[u].y);
+                v[u][2] = ldg16(vbase + o[u].z);
+                v[u][3] = ldg16(vbase + o[u].w);
+            }
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                float d[4];
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    float x[VEC];
+                    unpack16<T>(x, v[u][c]);
+                    float acc = 0.0f;
+#pragma unroll
+                    for (int i = 0; i < VEC; ++i) acc = fmaf(go[i], x[i], acc);
+                    d[c] = acc;
+                }
+                if (w[u].x != 0.0f) S::add(gvbase + o[u].x, w[u].x, go);
+                if (w[u].y != 0.0f) S::add(gvbase + o[u].y, w[u].y, go);
+                if (w[u].z != 0.0f) S::add(gvbase + o[u].z, w[u].z, go);
+                if (w[u].w != 0.0f) S::add(gvbase + o[u].w, w[u].w, go);
+#pragma unroll
+                for (int off = LPG / 2; off > 0; off >>= 1) {
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) d[c] += __shfl_xor_sync(0xffffffffu, d[c], off);
+                }
+                if (r == 0) s_dot[warp][(j + u) * GPW + g] = make_float4(d[0], d[1], d[2], d[3]);
+            }
+        }
+        __syncwarp();
+
+        // ---- phase 3: grad_attn and grad_loc of the samples this lane prepared
+#pragma unroll
+        for (int i = 0; i < NP; ++i) {
+            const int s = lane + 32 * i;
+            const int gs = s / CH, j = s % CH;
+            const int idx = base + j;
+            if (prep_ok[i] && idx < p.LK) {
+                const float4 dd = s_dot[warp][j * GPW + gs];
+                const unsigned m = f_mask[i];
+                const float s00 = (m & 1u) ? dd.x : 0.0f, s01 = (m & 2u) ? dd.y : 0.0f;
+                const float s10 = (m & 4u) ? dd.z : 0.0f, s11 = (m & 8u) ? dd.w : 0.0f;
+                const float lx = f_lx[i], ly = f_ly[i], hx = 1.0f - lx, hy = 1.0f - ly;
+                const float ga = hy * (hx * s00 + lx * s01) + ly * (hx * s10 + lx * s11);
+                const float dlx = hy * (s01 - s00) + ly * (s11 - s10);
+                const float dly = hx * (s10 - s00) + lx * (s11 - s01);
+                const int64_t e = prep_bqm[i] * p.LK + idx;
+                gattn[e] = Elem<T>::from_f(ga);
+                store_xy<T>(gloc + 2 * e, f_a[i] * f_W[i] * dlx, f_a[i] * f_H[i] * dly);
+            }
+        }
+        __syncwarp();
+    }
+}
+
+// Zero n16 16-byte words.
+__global__ void zero16_kernel(uint4 *p, int64_t n16) {
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n16; i += stride)
+        p[i] = make_uint4(0u, 0u, 0u, 0u);
+}
+
+// grad_value = round(workspace), 8 elements per thread.
+template <typename T>
+__global__ void convert8_kernel(const float4 *ws, uint4 *gv, int64_t n8) {
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n8; i += stride) {
+        const float4 a = ws[2 * i], b = ws[2 * i + 1];
+        const float v[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+        gv[i] = pack16<T>(v);
+    }
+}
+
+static unsigned stream_grid(int64_t n, int threads) {
+    const int64_t want = (n + threads - 1) / threads;
+    const int64_t cap = 152 * 16;  // a few waves of resident blocks on 152 SMs
+    return (unsigned)(want < 1 ? 1 : (want < cap ? want : cap));
+}
+
+cudaError_t launch_zero(void *p, int64_t bytes, cudaStream_t stream) {
+    const int64_t n16 = bytes / 16;
+    if (n16 == 0) return cudaSuccess;
+    zero16_kernel<<<stream_grid(n16, 256), 256, 0, stream>>>(reinterpret_cast<uint4 *>(p), n16);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_convert(const float *ws, void *gv, int64_t n, msda_dtype_t dt, cudaStream_t stream) {
+    const int64_t n8 = n / 8;
+    if (n8 == 0) return cudaSuccess;
+    const unsigned grid = stream_grid(n8, 256);
+    if (dt == MSDA_BF16)
+        convert8_kernel<__nv_bfloat16><<<grid, 256, 0, stream>>>(
+            reinterpret_cast<const float4 *>(ws), reinterpret_cast<uint4 *>(gv), n8);
+    else if (dt == MSDA_F16)
+        convert8_kernel<__half><<<grid, 256, 0, stream>>>(
+            reinterpret_cast<const float4 *>(ws), reinterpret_cast<uint4 *>(gv), n8);
+    else
+        return cudaErrorInvalidValue;
+    return cudaGetLastError();
+}
+
+template <typename T, bool F32ACC>
+static cudaError_t launch_backward_t(const Params &p, int lpg, cudaStream_t stream) {
+    const int gpw = 32 / lpg;
+    const int64_t warps = (p.triples + gpw - 1) / gpw;
+    const int64_t blocks = (warps + kWarpsPerBlock - 1) / kWarpsPerBlock;
+    if (blocks == 0) return cudaSuccess;
+    if (blocks > 0x7fffffff) return cudaErrorInvalidConfiguration;
+    const dim3 grid((unsigned)blocks);
+    switch (lpg) {
+        case 1: msda_backward_kernel<T, 1, F32ACC><<<grid, kThreads, 0, stream>>>(p); break;
+        case 2: msda_backward_kernel<T, 2, F32ACC><<<grid, kThreads, 0, stream>>>(p); break;
+        case 4: msda_backward_kernel<T, 4, F32ACC><<<grid, kThreads, 0, stream>>>(p); break;
+        case 8: msda_backward_kernel<T, 8, F32ACC><<<grid, kThreads, 0, stream>>>(p); break;
+        case 16: msda_backward_kernel<T, 16, F32ACC><<<grid, kThreads, 0, stream>>>(p); break;
+        case 32: msda_backward_kernel<T, 32, F32ACC><<<grid, kThreads, 0, stream>>>(p); break;
+        default: return cudaErrorInvalidValue;
+    }
+    return cudaGetLastError();
+}
+
+cudaError_t launch_backward(const Params &p, msda_dtype_t dt, bool f32acc, int lpg,
+                            cudaStream_t stream) {
+    switch (dt) {
+        case MSDA_F32: return launch_backward_t<float, true>(p, lpg, stream);
+        case MSDA_BF16:
+            return f32acc ? launch_backward_t<__nv_bfloat16, true>(p, lpg, stream)
+                          : launch_backward_t<__nv_bfloat16, false>(p, lpg, stream);
+        case MSDA_F16:
+            return f32acc ? launch_backward_t<__half, true>(p, lpg, stream)
+                          : launch_backward_t<__half, false>(p, lpg, stream);
+    }
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace msda

@@ -1,0 +1,166 @@
+// MSDA forward on sm_103a: gather-and-weight over L levels x K points.
+//
+// Work split. A "group" of LPG lanes owns one (b, q, m) query-head; each lane
+// owns 16 bytes (VEC channels) of the head's D channels, so one 16-byte load
+// per lane moves a whole D-channel corner vector per group. A warp holds
+// GPW = 32/LPG groups (consecutive heads of one query for the detector sizes),
+// and consecutive warps take consecutive queries: the query-block tiling of
+// the Efficient-MSDA summary page ("Two heuristics that do not apply": the
+// locality that matters comes from the tiling inside a query block).
+//
+// Per chunk of samples a warp runs two phases, separated by __syncwarp():
+//  1. prepare: each lane turns its own samples (2 per lane) into a descriptor
+//     -- four corner weights with the attention weight folded in (zero for a
+//     corner outside the map) and four corner row offsets -- from coalesced
+//     loads of sampling_locations and attention_weights, and stages it in
+//     shared memory. The coordinate arithmetic runs once per sample instead
+//     of once per lane of the group.
+//  2. gather: every lane of a group reads its group's descriptors (a
+//     broadcast) and issues four 16-byte loads per sample, U samples at a
+//     time so that 4U loads are in flight, accumulating in fp32 registers.
+// The group then writes its D output channels once (16 bytes per lane).
+#include "msda_common.cuh"
+
+namespace msda {
+
+template <typename T, int LPG>
+__global__ void __launch_bounds__(kThreads)
+msda_forward_kernel(const Params p) {
+    constexpr int VEC = Vec16<T>::N;
+    constexpr int GPW = 32 / LPG;            // groups per warp
+    constexpr int SPW = 64;                  // descriptors per warp per chunk
+    constexpr int CH = SPW / GPW;            // samples per group per chunk
+    constexpr int U = CH < 4 ? CH : 4;       // samples per gather step
+
+    __shared__ LevelTable lt;
+    __shared__ float4 s_w[kWarpsPerBlock][SPW];
+    __shared__ int4 s_o[kWarpsPerBlock][SPW];
+
+    load_level_table(lt, p);
+    __syncthreads();
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int g = lane / LPG, r = lane % LPG;
+    const int64_t t0 = ((int64_t)blockIdx.x * kWarpsPerBlock + warp) * GPW;
+    if (t0 >= p.triples) return;
+
+    // this lane's group
+    const int64_t t = t0 + g;
+    const bool active = t < p.triples;
+    Triple tr = triple_of(active ? t : t0, p);
+    const bool valid_q = active && tr.q >= 0 && tr.q < p.Q;
+    const T *vbase = reinterpret_cast<const T *>(p.value) +
+                     ((int64_t)tr.b * p.S * p.M + tr.m) * p.D + r * VEC;
+
+    // the triples whose samples this lane prepares in phase 1
+    int64_t prep_bqm[SPW / 32];
+    bool prep_ok[SPW / 32];
+#pragma unroll
+    for (int i = 0; i < SPW / 32; ++i) {
+        const int s = lane + 32 * i;
+        const int64_t ts = t0 + s / CH;
+        prep_ok[i] = ts < p.triples;
+        Triple trs = triple_of(prep_ok[i] ? ts : t0, p);
+        prep_ok[i] = prep_ok[i] && trs.q >= 0 && trs.q < p.Q;
+        prep_bqm[i] = trs.bqm;
+    }
+
+    const T *loc = reinterpret_cast<const T *>(p.loc);
+    const T *attn = reinterpret_cast<const T *>(p.attn);
+
+    float acc[VEC];
+#pragma unroll
+    for (int i = 0; i < VEC; ++i) acc[i] = 0.0f;
+
+    for (int base = 0; base < p.LK; base += CH) {
+        // ---- phase 1: descriptors
+#pragma unroll
+        for (int i = 0; i < SPW / 32; ++i) {
+            const int s = lane + 32 * i;
+            const int gs = s / CH, j = s % CH;
+            const int idx = base + j;
+            float4 w = make_float4(0.f, 0.f, 0.f, 0.f);
+            int4 o = make_int4(0, 0, 0, 0);
+            if (prep_ok[i] && idx < p.LK) {
+                const int64_t e = prep_bqm[i] * p.LK + idx;
+                const float2 xy = load_xy<T>(loc + 2 * e);
+                const float a = load_scalar<T>(attn + e);
+                const int l = level_of(idx, p.inv_K);
+                SampleGeom sg;
+                sample_geometry(sg, xy.x, xy.y, lt, l);
+                const float hx = 1.0f - sg.lx, hy = 1.0f - sg.ly;
+                const float ahy = a * hy, aly = a * sg.ly;
+                w.x = (sg.vx0 && sg.vy0) ? ahy * hx : 0.0f;
+                w.y = (sg.vx1 && sg.vy0) ? ahy * sg.lx : 0.0f;
+                w.z = (sg.vx0 && sg.vy1) ? aly * hx : 0.0f;
+                w.w = (sg.vx1 && sg.vy1) ? aly * sg.lx : 0.0f;
+                o = make_int4(sg.row[0] * p.MD, sg.row[1] * p.MD, sg.row[2] * p.MD,
+                              sg.row[3] * p.MD);
+            }
+            // interleaved [sample][group]: the GPW groups read adjacent words
+            s_w[warp][j * GPW + gs] = w;
+            s_o[warp][j * GPW + gs] = o;
+        }
+        __syncwarp();
+
+        // ---- phase 2: gather
+        const int n = min(CH, p.LK - base);
+        for (int j = 0; j < n; j += U) {
+            float4 w[U];
+            uint4 v[U][4];
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                w[u] = s_w[warp][(j + u) * GPW + g];
+                const int4 o = s_o[warp][(j + u) * GPW + g];
+                v[u][0] = ldg16(vbase + o.x);
+                v[u][1] = ldg16(vbase + o.y);
+                v[u][2] = ldg16(vbase + o.z);
+                v[u][3] = ldg16(vbase + o.w);
+            }
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                fma16<T>(acc, w[u].x, v[u][0]);
+                fma16<T>(acc, w[u].y, v[u][1]);
+                fma16<T>(acc, w[u].z, v[u][2]);
+                fma16<T>(acc, w[u].w, v[u][3]);
+            }
+        }
+        __syncwarp();
+    }
+
+    if (valid_q) {
+        T *o = reinterpret_cast<T *>(p.out) + tr.bqm * p.D + r * VEC;
+        *reinterpret_cast<uint4 *>(o) = pack16<T>(acc);
+    }
+}
+
+template <typename T>
+static cudaError_t launch_forward_t(const Params &p, int lpg, cudaStream_t stream) {
+    const int gpw = 32 / lpg;
+    const int64_t warps = (p.triples + gpw - 1) / gpw;
+    const int64_t blocks = (warps + kWarpsPerBlock - 1) / kWarpsPerBlock;
+    if (blocks == 0) return cudaSuccess;
+    if (blocks > 0x7fffffff) return cudaErrorInvalidConfiguration;
+    const dim3 grid((unsigned)blocks);
+    switch (lpg) {
+        case 1: msda_forward_kernel<T, 1><<<grid, kThreads, 0, stream>>>(p); break;
+        case 2: msda_forward_kernel<T, 2><<<grid, kThreads, 0, stream>>>(p); break;
+        case 4: msda_forward_kernel<T, 4><<<grid, kThreads, 0, stream>>>(p); break;
+        case 8: msda_forward_kernel<T, 8><<<grid, kThreads, 0, stream>>>(p); break;
+        case 16: msda_forward_kernel<T, 16><<<grid, kThreads, 0, stream>>>(p); break;
+        case 32: msda_forward_kernel<T, 32><<<grid, kThreads, 0, stream>>>(p); break;
+        default: return cudaErrorInvalidValue;
+    }
+    return cudaGetLastError();
+}
+
+cudaError_t launch_forward(const Params &p, msda_dtype_t dt, int lpg, cudaStream_t stream) {
+    switch (dt) {
+        case MSDA_F32: return launch_forward_t<float>(p, lpg, stream);
+        case MSDA_BF16: return launch_forward_t<__nv_bfloat16>(p, lpg, stream);
+        case MSDA_F16: return launch_forward_t<__half>(p, lpg, stream);
+    }
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace msda

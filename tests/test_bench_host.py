@@ -1,0 +1,79 @@
+"""CPU checks of bench.py's host logic: the max-over-ranks timing and the
+whole-job sum on two gloo ranks, argument rules, and the reference arm."""
+import json
+import os
+import subprocess
+import sys
+
+import pytest
+import torch.multiprocessing as mp
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _rank_main(rank, world, port, out):
+    import torch.distributed as dist
+    sys.path.insert(0, ROOT)
+    import bench
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    # rank r processes (r+1)*100 queries in (1+r) seconds
+    qps, slowest, total = bench.job_throughput((rank + 1) * 100.0, 1.0 + rank)
+    bench.barrier()
+    out[rank] = (qps, slowest, total)
+    dist.destroy_process_group()
+
+
+def test_two_rank_timing_reduction():
+    import random
+    port = 29500 + random.randint(0, 2000)
+    with mp.Manager() as m:
+        out = m.dict()
+        mp.spawn(_rank_main, args=(2, port, out), nprocs=2, join=True)
+        res = dict(out)
+    for r in (0, 1):
+        qps, slowest, total = res[r]
+        assert slowest == 2.0 and total == 300.0
+        assert qps == pytest.approx(150.0)      # all units over the slowest rank's time
+
+
+def test_single_process_reduction_is_identity():
+    sys.path.insert(0, ROOT)
+    import bench
+    assert bench.job_throughput(10.0, 2.0) == (5.0, 2.0, 10.0)
+
+
+def test_argument_rules():
+    sys.path.insert(0, ROOT)
+    import bench
+    a = bench.parse_args([])
+    assert a.gpus == 1 and a.warmup >= 3 and a.impl == "ours"
+    with pytest.raises(SystemExit):
+        bench.parse_args(["--warmup", "2"])
+
+
+def test_traffic_figure_needs_matching_kernel_sources(tmp_path):
+    sys.path.insert(0, ROOT)
+    import bench
+    h = bench.kernel_source_hash()
+    assert len(h) == 16
+    assert bench.profiled_traffic("no_such_kernel") is None
+
+
+def test_reference_arm_prints_its_line():
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
+                        "--steps", "3", "--warmup", "3"], capture_output=True, text=True,
+                       timeout=600, cwd=ROOT)
+    assert r.returncode == 0, r.stderr
+    line = json.loads(r.stdout.strip().splitlines()[-1])
+    assert line["impl"] == "reference" and line["value"] > 0
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] >= 1
+    assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["unit"] == "queries/s"
+
+
+def test_reference_arm_other_ranks_exit_quietly():
+    env = dict(os.environ, RANK="1", WORLD_SIZE="2", LOCAL_RANK="1")
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
+                        "--steps", "3", "--warmup", "3"], capture_output=True, text=True,
+                       timeout=120, cwd=ROOT, env=env)
+    assert r.returncode == 0 and r.stdout.strip() == ""

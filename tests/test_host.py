@@ -1,0 +1,146 @@
+"""Host-side checks of libmsda that need no GPU.
+
+The library must build, load, export every entry point include/msda.h
+declares, and reject invalid arguments on the host before any CUDA call (so
+these run on a machine without a GPU). No compute call is made here.
+"""
+import ctypes
+import os
+import re
+
+import pytest
+import torch
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def so():
+    from scale_deformable_attention_msda_gb300 import binding, build
+    build.build()
+    return binding.load()
+
+
+def _declared_symbols():
+    names = []
+    for h in sorted(os.listdir(os.path.join(ROOT, "include"))):
+        if h.endswith(".h"):
+            text = open(os.path.join(ROOT, "include", h)).read()
+            names += re.findall(r"MSDA_API\s+[\w\s\*]+?\b(\w+)\s*\(", text)
+    return names
+
+
+def test_header_declares_the_api():
+    names = _declared_symbols()
+    from scale_deformable_attention_msda_gb300.binding import EXPORTED
+    for n in EXPORTED:
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(so):
+    for name in _declared_symbols():
+        assert hasattr(so, name), name
+
+
+def test_library_exports_nothing_else(so):
+    import subprocess
+    from scale_deformable_attention_msda_gb300 import build
+    out = subprocess.run(["nm", "-D", "--defined-only", build.LIBRARY], capture_output=True,
+                         text=True, check=True).stdout
+    exported = {line.split()[-1] for line in out.splitlines() if " T " in line}
+    assert exported == set(_declared_symbols())
+
+
+def test_status_strings_and_version(so):
+    for s in range(7):
+        assert so.msda_status_string(s)
+    assert so.msda_status_string(99) == b"unknown status"
+    assert so.msda_version() >= 100
+
+
+def _dims(**kw):
+    from scale_deformable_attention_msda_gb300.binding import msda_dims_t
+    d = dict(B=2, S=22223, Q=300, M=8, D=32, L=4, K=4)
+    d.update(kw)
+    return msda_dims_t(**d)
+
+
+FAKE = 0x10000   # 16-byte aligned address; every call below fails validation or is
+                 # empty, so no kernel is ever launched with it
+
+
+def _fwd(so, dims, dtype=0, value=FAKE, shapes=FAKE, starts=FAKE, loc=FAKE, attn=FAKE,
+         out=FAKE, order=None):
+    vp = ctypes.c_void_p
+    return so.msda_forward(vp(value), vp(shapes), vp(starts), vp(loc), vp(attn), vp(order),
+                           vp(out), ctypes.byref(dims) if dims is not None else None, dtype,
+                           vp(0))
+
+
+def _bwd(so, dims, dtype=0, accum=1, ws=FAKE, ws_bytes=1 << 40, grad_value=FAKE, **kw):
+    vp = ctypes.c_void_p
+    return so.msda_backward(vp(FAKE), vp(FAKE), vp(FAKE), vp(FAKE), vp(FAKE), vp(None),
+                            vp(FAKE), vp(grad_value), vp(FAKE), vp(FAKE), vp(ws),
+                            ctypes.c_size_t(ws_bytes), accum, ctypes.byref(dims), dtype, vp(0))
+
+
+def test_validation_errors_before_any_launch(so):
+    assert _fwd(so, None) == 1                                   # NULL dims
+    assert _fwd(so, _dims(), dtype=7) == 3                       # bad dtype
+    assert _fwd(so, _dims(L=17)) == 2                            # too many levels
+    assert _fwd(so, _dims(L=0)) == 2
+    assert _fwd(so, _dims(K=0)) == 2
+    assert _fwd(so, _dims(D=12)) == 2                            # not a power-of-two multiple of 4
+    assert _fwd(so, _dims(D=256)) == 2                           # fp32: D/4 = 64 lanes > 32
+    assert _fwd(so, _dims(S=0)) == 2
+    assert _fwd(so, _dims(B=-1)) == 2
+    assert _fwd(so, _dims(S=2 ** 23, M=8, D=32)) == 2            # S*M*D >= 2^31
+    assert _fwd(so, _dims(), value=None) == 1
+    assert _fwd(so, _dims(), loc=None) == 1
+    assert _fwd(so, _dims(), out=None) == 1
+    assert _fwd(so, _dims(), value=FAKE + 4) == 4                # value not 16-byte aligned
+    assert _fwd(so, _dims(), out=FAKE + 8) == 4
+    assert _fwd(so, _dims(), loc=FAKE + 4) == 4                  # fp32 loc pairs need 8 bytes
+    # bf16 pairs need only 4-byte alignment: the call gets past that check and
+    # stops at the missing output (no call here reaches a launch)
+    assert _fwd(so, _dims(), dtype=1, loc=FAKE + 4, out=None) == 1
+    assert _fwd(so, _dims(), shapes=FAKE + 4) == 4
+    assert _fwd(so, _dims(), order=FAKE + 2) == 4
+
+
+def test_empty_problems_are_valid_and_launch_nothing(so):
+    assert _fwd(so, _dims(B=0)) == 0
+    assert _fwd(so, _dims(Q=0)) == 0
+    assert _fwd(so, _dims(B=0), value=None, loc=None, attn=None, out=None) == 0
+    assert _bwd(so, _dims(B=0)) == 0
+
+
+def test_backward_workspace_rules(so):
+    d = _dims()
+    n = 2 * 22223 * 8 * 32
+    assert so.msda_backward_workspace_bytes(ctypes.byref(d), 1, 1) == 4 * n     # bf16, fp32 buffer
+    assert so.msda_backward_workspace_bytes(ctypes.byref(d), 2, 1) == 4 * n     # f16, fp32 buffer
+    assert so.msda_backward_workspace_bytes(ctypes.byref(d), 1, 0) == 0         # native
+    assert so.msda_backward_workspace_bytes(ctypes.byref(d), 0, 1) == 0         # fp32 data
+    assert so.msda_backward_workspace_bytes(ctypes.byref(_dims(L=0)), 1, 1) == 0
+    assert _bwd(so, d, dtype=1, accum=1, ws=None) == 5
+    assert _bwd(so, d, dtype=1, accum=1, ws_bytes=4 * n - 1) == 5
+    assert _bwd(so, d, dtype=1, accum=1, ws=FAKE + 8, ws_bytes=4 * n) == 4
+    assert _bwd(so, d, dtype=1, accum=5) == 3
+    assert _bwd(so, d, grad_value=None) == 1
+
+
+def test_binding_refuses_cpu_tensors(so):
+    from scale_deformable_attention_msda_gb300 import binding
+    v = torch.zeros(1, 80, 2, 8)
+    loc = torch.zeros(1, 4, 2, 2, 2, 2)
+    attn = torch.zeros(1, 4, 2, 2, 2)
+    shapes = torch.tensor([[8, 8], [4, 4]])
+    starts = torch.tensor([0, 64])
+    with pytest.raises(ValueError, match="CUDA"):
+        binding.msda_forward(v, shapes, starts, loc, attn)
+
+
+def test_graft_entry_build():
+    import __graft_entry__
+    __graft_entry__.build()
