@@ -46,39 +46,74 @@ __device__ __forceinline__ void red_add_v4_f16x2(void *p, uint4 v) {
                  : "memory");
 }
 
-// grad_value[p .. p+VEC) += w * g for one lane's VEC channels.
-template <typename T, bool F32ACC> struct Scatter;
-template <> struct Scatter<float, true> {
+// One lane's share of grad_value[row, 0..D) += w * g, where `row` points at
+// the D channels of one head at one corner pixel. Each lane holds the grad_out
+// channels it scatters (sc, loaded once per query-head by load_scatter_g), and
+// every instruction of the group covers whole 32-byte sectors:
+//  - fp32 data: lane r adds channels [4r, 4r+4); LPG lanes cover D floats.
+//  - 16-bit data, fp32 workspace: two 16-byte adds per lane, channels
+//    [4r, 4r+4) then [4 LPG + 4r, ...), so each instruction writes 16 LPG
+//    contiguous bytes per group (a lane's gathered 8 channels would leave
+//    every other 16 bytes of a sector untouched).
+//  - 16-bit data, native: lane r adds its 8 channels [8r, 8r+8) in one
+//    bf16x2/f16x2 instruction.
+template <typename T, bool F32ACC, int LPG> struct Scatter;
+template <int LPG> struct Scatter<float, true, LPG> {
     using Acc = float;
-    static __device__ __forceinline__ void add(float *p, float w, const float *g) {
-        red_add_v4_f32(p, w * g[0], w * g[1], w * g[2], w * g[3]);
+    static constexpr int NSC = 4;
+    static __device__ __forceinline__ void add(float *row, float w, const float *sc, int r) {
+        red_add_v4_f32(row + 4 * r, w * sc[0], w * sc[1], w * sc[2], w * sc[3]);
     }
 };
-template <typename T> struct Scatter<T, true> {  // 16-bit data, fp32 workspace
+template <typename T, int LPG> struct Scatter<T, true, LPG> {
     using Acc = float;
-    static __device__ __forceinline__ void add(float *p, float w, const float *g) {
-        red_add_v4_f32(p, w * g[0], w * g[1], w * g[2], w * g[3]);
-        red_add_v4_f32(p + 4, w * g[4], w * g[5], w * g[6], w * g[7]);
+    static constexpr int NSC = 8;
+    static __device__ __forceinline__ void add(float *row, float w, const float *sc, int r) {
+        red_add_v4_f32(row + 4 * r, w * sc[0], w * sc[1], w * sc[2], w * sc[3]);
+        red_add_v4_f32(row + 4 * LPG + 4 * r, w * sc[4], w * sc[5], w * sc[6], w * sc[7]);
     }
 };
-template <> struct Scatter<__nv_bfloat16, false> {
+template <int LPG> struct Scatter<__nv_bfloat16, false, LPG> {
     using Acc = __nv_bfloat16;
-    static __device__ __forceinline__ void add(__nv_bfloat16 *p, float w, const float *g) {
+    static constexpr int NSC = 8;
+    static __device__ __forceinline__ void add(__nv_bfloat16 *row, float w, const float *sc, int r) {
         float t[8];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) t[i] = w * g[i];
-        red_add_v4_bf16x2(p, pack16<__nv_bfloat16>(t));
+        for (int i = 0; i < 8; ++i) t[i] = w * sc[i];
+        red_add_v4_bf16x2(row + 8 * r, pack16<__nv_bfloat16>(t));
     }
 };
-template <> struct Scatter<__half, false> {
+template <int LPG> struct Scatter<__half, false, LPG> {
     using Acc = __half;
-    static __device__ __forceinline__ void add(__half *p, float w, const float *g) {
+    static constexpr int NSC = 8;
+    static __device__ __forceinline__ void add(__half *row, float w, const float *sc, int r) {
         float t[8];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) t[i] = w * g[i];
-        red_add_v4_f16x2(p, pack16<__half>(t));
+        for (int i = 0; i < 8; ++i) t[i] = w * sc[i];
+        red_add_v4_f16x2(row + 8 * r, pack16<__half>(t));
     }
 };
+
+// 8 bytes of T (4 channels) as fp32.
+template <typename T> __device__ __forceinline__ void load4(float *v, const T *p) {
+    const uint2 u = __ldg(reinterpret_cast<const uint2 *>(p));
+    float x[8];
+    unpack16<T>(x, make_uint4(u.x, u.y, 0u, 0u));
+#pragma unroll
+    for (int i = 0; i < 4; ++i) v[i] = x[i];
+}
+
+// The grad_out channels lane r scatters (see Scatter).
+template <typename T, bool F32ACC, int LPG>
+__device__ __forceinline__ void load_scatter_g(float *sc, const float *go, const T *grow, int r) {
+    if constexpr (F32ACC && sizeof(T) == 2) {
+        load4<T>(sc, grow + 4 * r);
+        load4<T>(sc + 4, grow + 4 * LPG + 4 * r);
+    } else {
+#pragma unroll
+        for (int i = 0; i < Vec16<T>::N; ++i) sc[i] = go[i];
+    }
+}
 
 template <typename T> __device__ __forceinline__ void store_xy(T *p, float x, float y);
 template <> __device__ __forceinline__ void store_xy<float>(float *p, float x, float y) {
@@ -100,7 +135,7 @@ msda_backward_kernel(const Params p) {
     constexpr int CH = SPW / GPW;
     constexpr int NP = SPW / 32;             // samples each lane prepares per chunk
     constexpr int U = CH < 2 ? CH : 2;
-    using S = Scatter<T, F32ACC>;
+    using S = Scatter<T, F32ACC, LPG>;
     using Acc = typename S::Acc;
 
     __shared__ LevelTable lt;
@@ -120,30 +155,31 @@ msda_backward_kernel(const Params p) {
     const bool active = t < p.triples;
     const Triple tr = triple_of(active ? t : t0, p);
     const bool valid_q = active && tr.q >= 0 && tr.q < p.Q;
-    const int64_t vrow = ((int64_t)tr.b * p.S * p.M + tr.m) * p.D + r * VEC;
-    const T *vbase = reinterpret_cast<const T *>(p.value) + vrow;
-    Acc *gvbase = reinterpret_cast<Acc *>(p.grad_value) + vrow;
+    const int64_t head = ((int64_t)tr.b * p.S * p.M + tr.m) * p.D;    // row 0 of this head
+    const T *vbase = reinterpret_cast<const T *>(p.value) + head + r * VEC;
+    Acc *gvhead = reinterpret_cast<Acc *>(p.grad_value) + head;
 
-    // this lane's slice of grad_out (zero for a group with nothing to do)
-    float go[VEC];
+    // grad_out of this query-head: the lane's gathered channels (for the dot
+    // products) and the channels it scatters (zero for a group with no work)
+    float go[VEC], sc[S::NSC];
     if (valid_q) {
-        unpack16<T>(go, ldg16(reinterpret_cast<const T *>(p.grad_out) + tr.bqm * p.D + r * VEC));
+        const T *grow = reinterpret_cast<const T *>(p.grad_out) + tr.bqm * p.D;
+        unpack16<T>(go, ldg16(grow + r * VEC));
+        load_scatter_g<T, F32ACC, LPG>(sc, go, grow, r);
     } else {
 #pragma unroll
         for (int i = 0; i < VEC; ++i) go[i] = 0.0f;
+#pragma unroll
+        for (int i = 0; i < S::NSC; ++i) sc[i] = 0.0f;
     }
 
-    int64_t prep_bqm[NP];
-    bool prep_ok[NP];
-#pragma unroll
-    for (int i = 0; i < NP; ++i) {
-        const int s = lane + 32 * i;
-        const int64_t ts = t0 + s / CH;
-        prep_ok[i] = ts < p.triples;
-        const Triple trs = triple_of(prep_ok[i] ? ts : t0, p);
-        prep_ok[i] = prep_ok[i] && trs.q >= 0 && trs.q < p.Q;
-        prep_bqm[i] = trs.bqm;
-    }
+    // phase-1/3 mapping as in the forward: slot lane + 32*i is sample
+    // pj + i*LPG of group pg = lane % GPW
+    const int pg = lane % GPW, pj = lane / GPW;
+    const int64_t tp = t0 + pg;
+    bool prep_ok = tp < p.triples;
+    const Triple trp = triple_of(prep_ok ? tp : t0, p);
+    prep_ok = prep_ok && trp.q >= 0 && trp.q < p.Q;
 
     const T *loc = reinterpret_cast<const T *>(p.loc);
     const T *attn = reinterpret_cast<const T *>(p.attn);
@@ -156,15 +192,13 @@ msda_backward_kernel(const Params p) {
         unsigned f_mask[NP];
 #pragma unroll
         for (int i = 0; i < NP; ++i) {
-            const int s = lane + 32 * i;
-            const int gs = s / CH, j = s % CH;
-            const int idx = base + j;
+            const int idx = base + pj + i * LPG;
             float4 w = make_float4(0.f, 0.f, 0.f, 0.f);
             int4 o = make_int4(0, 0, 0, 0);
             f_lx[i] = f_ly[i] = f_a[i] = f_W[i] = f_H[i] = 0.0f;
             f_mask[i] = 0u;
-            if (prep_ok[i] && idx < p.LK) {
-                const int64_t e = prep_bqm[i] * p.LK + idx;
+            if (prep_ok && idx < p.LK) {
+                const int64_t e = trp.bqm * p.LK + idx;
                 const float2 xy = load_xy<T>(loc + 2 * e);
                 const float a = load_scalar<T>(attn + e);
                 const int l = level_of(idx, p.inv_K);
@@ -187,8 +221,8 @@ msda_backward_kernel(const Params p) {
                 f_H[i] = lt.Hf[l];
                 f_mask[i] = m;
             }
-            s_w[warp][j * GPW + gs] = w;
-            s_o[warp][j * GPW + gs] = o;
+            s_w[warp][lane + 32 * i] = w;
+            s_o[warp][lane + 32 * i] = o;
         }
         __syncwarp();
 
@@ -219,10 +253,10 @@ msda_backward_kernel(const Params p) {
                     for (int i = 0; i < VEC; ++i) acc = fmaf(go[i], x[i], acc);
                     d[c] = acc;
                 }
-                if (w[u].x != 0.0f) S::add(gvbase + o[u].x, w[u].x, go);
-                if (w[u].y != 0.0f) S::add(gvbase + o[u].y, w[u].y, go);
-                if (w[u].z != 0.0f) S::add(gvbase + o[u].z, w[u].z, go);
-                if (w[u].w != 0.0f) S::add(gvbase + o[u].w, w[u].w, go);
+                if (w[u].x != 0.0f) S::add(gvhead + o[u].x, w[u].x, sc, r);
+                if (w[u].y != 0.0f) S::add(gvhead + o[u].y, w[u].y, sc, r);
+                if (w[u].z != 0.0f) S::add(gvhead + o[u].z, w[u].z, sc, r);
+                if (w[u].w != 0.0f) S::add(gvhead + o[u].w, w[u].w, sc, r);
 #pragma unroll
                 for (int off = LPG / 2; off > 0; off >>= 1) {
 #pragma unroll
@@ -236,11 +270,9 @@ msda_backward_kernel(const Params p) {
         // ---- phase 3: grad_attn and grad_loc of the samples this lane prepared
 #pragma unroll
         for (int i = 0; i < NP; ++i) {
-            const int s = lane + 32 * i;
-            const int gs = s / CH, j = s % CH;
-            const int idx = base + j;
-            if (prep_ok[i] && idx < p.LK) {
-                const float4 dd = s_dot[warp][j * GPW + gs];
+            const int idx = base + pj + i * LPG;
+            if (prep_ok && idx < p.LK) {
+                const float4 dd = s_dot[warp][lane + 32 * i];
                 const unsigned m = f_mask[i];
                 const float s00 = (m & 1u) ? dd.x : 0.0f, s01 = (m & 2u) ? dd.y : 0.0f;
                 const float s10 = (m & 4u) ? dd.z : 0.0f, s11 = (m & 8u) ? dd.w : 0.0f;
@@ -248,7 +280,7 @@ msda_backward_kernel(const Params p) {
                 const float ga = hy * (hx * s00 + lx * s01) + ly * (hx * s10 + lx * s11);
                 const float dlx = hy * (s01 - s00) + ly * (s11 - s10);
                 const float dly = hx * (s10 - s00) + lx * (s11 - s01);
-                const int64_t e = prep_bqm[i] * p.LK + idx;
+                const int64_t e = trp.bqm * p.LK + idx;
                 gattn[e] = Elem<T>::from_f(ga);
                 store_xy<T>(gloc + 2 * e, f_a[i] * f_W[i] * dlx, f_a[i] * f_H[i] * dly);
             }

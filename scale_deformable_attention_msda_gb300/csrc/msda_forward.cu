@@ -52,18 +52,15 @@ msda_forward_kernel(const Params p) {
     const T *vbase = reinterpret_cast<const T *>(p.value) +
                      ((int64_t)tr.b * p.S * p.M + tr.m) * p.D + r * VEC;
 
-    // the triples whose samples this lane prepares in phase 1
-    int64_t prep_bqm[SPW / 32];
-    bool prep_ok[SPW / 32];
-#pragma unroll
-    for (int i = 0; i < SPW / 32; ++i) {
-        const int s = lane + 32 * i;
-        const int64_t ts = t0 + s / CH;
-        prep_ok[i] = ts < p.triples;
-        Triple trs = triple_of(prep_ok[i] ? ts : t0, p);
-        prep_ok[i] = prep_ok[i] && trs.q >= 0 && trs.q < p.Q;
-        prep_bqm[i] = trs.bqm;
-    }
+    // Phase 1 fills descriptor slot lane + 32*i, stored in [sample][group]
+    // order, so consecutive lanes write consecutive 16-byte words (no bank
+    // conflicts). Slot lane + 32*i belongs to group lane % GPW and sample
+    // lane / GPW + i*LPG of the chunk: each lane prepares one triple's samples.
+    const int pg = lane % GPW, pj = lane / GPW;
+    const int64_t tp = t0 + pg;
+    bool prep_ok = tp < p.triples;
+    const Triple trp = triple_of(prep_ok ? tp : t0, p);
+    prep_ok = prep_ok && trp.q >= 0 && trp.q < p.Q;
 
     const T *loc = reinterpret_cast<const T *>(p.loc);
     const T *attn = reinterpret_cast<const T *>(p.attn);
@@ -76,13 +73,12 @@ msda_forward_kernel(const Params p) {
         // ---- phase 1: descriptors
 #pragma unroll
         for (int i = 0; i < SPW / 32; ++i) {
-            const int s = lane + 32 * i;
-            const int gs = s / CH, j = s % CH;
+            const int j = pj + i * LPG;
             const int idx = base + j;
             float4 w = make_float4(0.f, 0.f, 0.f, 0.f);
             int4 o = make_int4(0, 0, 0, 0);
-            if (prep_ok[i] && idx < p.LK) {
-                const int64_t e = prep_bqm[i] * p.LK + idx;
+            if (prep_ok && idx < p.LK) {
+                const int64_t e = trp.bqm * p.LK + idx;
                 const float2 xy = load_xy<T>(loc + 2 * e);
                 const float a = load_scalar<T>(attn + e);
                 const int l = level_of(idx, p.inv_K);
@@ -97,9 +93,8 @@ msda_forward_kernel(const Params p) {
                 o = make_int4(sg.row[0] * p.MD, sg.row[1] * p.MD, sg.row[2] * p.MD,
                               sg.row[3] * p.MD);
             }
-            // interleaved [sample][group]: the GPW groups read adjacent words
-            s_w[warp][j * GPW + gs] = w;
-            s_o[warp][j * GPW + gs] = o;
+            s_w[warp][lane + 32 * i] = w;     // == [j * GPW + pg]
+            s_o[warp][lane + 32 * i] = o;
         }
         __syncwarp();
 
