@@ -167,34 +167,38 @@ def measured_hbm_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
+KERNEL_SOURCES = {"msda_forward_kernel": ("msda_common.cuh", "msda_forward.cu"),
+                  "msda_backward_kernel": ("msda_common.cuh", "msda_backward.cu")}
+
+
+def kernel_source_hash(kernel: str) -> str:
+    """sha256 prefix of the source files that define `kernel`."""
+    import hashlib
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "scale_deformable_attention_msda_gb300", "csrc")
+    for name in KERNEL_SOURCES[kernel]:
+        h.update(name.encode())
+        h.update(open(os.path.join(csrc, name), "rb").read())
+    return h.hexdigest()[:16]
+
+
 def profiled_traffic(kernel: str):
     """DRAM bytes per launch of `kernel` from the committed ncu summary, or None.
 
     profiles/<kernel>_encoder.md carries a line
-    `traffic_bytes_per_launch: N  source_sha256: H`; it counts only while the
-    kernel sources still hash to H."""
-    import hashlib
+    `traffic_bytes_per_launch: N  source_sha256: H`; the figure counts only
+    while the kernel's sources still hash to H (else the kernel has changed
+    since the counters were taken)."""
+    import re
     path = os.path.join(ROOT, "profiles", f"{kernel}_encoder.md")
     try:
         text = open(path).read()
     except OSError:
         return None
-    import re
     m = re.search(r"traffic_bytes_per_launch:\s*(\d+)\s+source_sha256:\s*([0-9a-f]+)", text)
-    if not m:
+    if not m or kernel not in KERNEL_SOURCES:
         return None
-    return int(m.group(1)) if m.group(2) == kernel_source_hash() else None
-
-
-def kernel_source_hash() -> str:
-    import hashlib
-    h = hashlib.sha256()
-    csrc = os.path.join(ROOT, "scale_deformable_attention_msda_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
-        if name.endswith((".cu", ".cuh")):
-            h.update(name.encode())
-            h.update(open(os.path.join(csrc, name), "rb").read())
-    return h.hexdigest()[:16]
+    return int(m.group(1)) if m.group(2) == kernel_source_hash(kernel) else None
 
 
 # ---------------------------------------------------------- CPU baseline
@@ -316,7 +320,7 @@ def run_ours(args):
     h2d = sum(t.numel() * t.element_size() for t in host.values())
     d2h = sum(t.numel() * t.element_size() for t in host_out.values())
     e2e_ms = []
-    for i in range(args.e2e_steps + 3):
+    for i in range(args.e2e_steps + 3 if args.e2e_steps > 0 else 0):
         flush.fill_(i & 0xff)
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
@@ -338,7 +342,12 @@ def run_ours(args):
         torch.cuda.synchronize()
         if i >= 3:
             e2e_ms.append(e0.elapsed_time(e1))
-    e2e_qps, _, _ = job_throughput(w.B * w.Q * len(e2e_ms), sum(e2e_ms) / 1e3, dev)
+    e2e = None
+    if e2e_ms:
+        e2e_qps, _, _ = job_throughput(w.B * w.Q * len(e2e_ms), sum(e2e_ms) / 1e3, dev)
+        e2e = {"value": round(e2e_qps, 1), "unit": UNIT, "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h, "steps": len(e2e_ms),
+               "ms_per_step": round(statistics.fmean(e2e_ms), 4)}
 
     # ---- roofline of the dominant kernel
     cb = wl.compulsory_bytes(w)
@@ -387,12 +396,10 @@ def run_ours(args):
             "kernels": kernels,
             "roofline": roofline,
             "cpu_baseline": cpu,
-            "e2e": {"value": round(e2e_qps, 1), "unit": UNIT, "h2d_bytes_per_step": h2d,
-                    "d2h_bytes_per_step": d2h, "steps": len(e2e_ms),
-                    "ms_per_step": round(statistics.fmean(e2e_ms), 4)},
+            "e2e": e2e,
             "gpu_launches": launches_per_step * args.steps,
             "clocks": clocks,
-            "kernel_source_sha256": kernel_source_hash(),
+            "kernel_source_sha256": {k: kernel_source_hash(k) for k in KERNEL_SOURCES},
         }
         print(json.dumps(result), flush=True)
     if world > 1:

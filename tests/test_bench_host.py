@@ -55,8 +55,8 @@ def test_argument_rules():
 def test_traffic_figure_needs_matching_kernel_sources(tmp_path):
     sys.path.insert(0, ROOT)
     import bench
-    h = bench.kernel_source_hash()
-    assert len(h) == 16
+    h = bench.kernel_source_hash("msda_backward_kernel")
+    assert len(h) == 16 and h != bench.kernel_source_hash("msda_forward_kernel")
     assert bench.profiled_traffic("no_such_kernel") is None
 
 
