@@ -182,6 +182,37 @@ MSDA_API msda_status_t msda_backward_finish(const void *workspace, size_t worksp
                                             const msda_dims_t *dims, msda_dtype_t dtype,
                                             void *stream);
 
+/* Size of the fp32 accumulator that msda_backward_static_workspace keeps
+ * inside the library: 64 MiB, enough for B*S*M*D <= 16,777,216 (for example
+ * the Deformable-DETR encoder shape with B = 2). */
+#define MSDA_STATIC_WORKSPACE_BYTES ((size_t)64 << 20)
+
+/* msda_backward for callers that cannot allocate device memory when they call
+ * (an operator plugin whose engine owns all device memory and offers no
+ * scratch, or an application that allows no device allocation after start-up).
+ * The pages describe no such entry point; it exists for those callers only.
+ * It computes what msda_backward computes with MSDA_ACC_FP32_BUFFER, using as
+ * its fp32 workspace a fixed MSDA_STATIC_WORKSPACE_BYTES array that belongs to
+ * the library, and it allocates nothing. Arguments as msda_backward, without
+ * the workspace and the accumulation mode.
+ * - Returns MSDA_ERR_WORKSPACE, before any launch, when a 16-bit problem needs
+ *   more than MSDA_STATIC_WORKSPACE_BYTES (B*S*M*D*4 bytes). fp32 data needs no
+ *   workspace and has no such limit.
+ * - The first call on each device looks up the array's device address with
+ *   that device current (MSDA_ERR_CUDA if the lookup fails); make that first
+ *   call before any stream capture begins.
+ * - Every call shares the one array. Each call clears the part it uses, but
+ *   calls that overlap on the GPU (other streams, other host threads) race on
+ *   it: the caller must order them.
+ * - The array occupies device memory on every GPU where this entry point has
+ *   run, until the process exits. */
+MSDA_API msda_status_t msda_backward_static_workspace(
+    const void *value, const int64_t *spatial_shapes, const int64_t *level_start_index,
+    const void *sampling_locations, const void *attention_weights,
+    const int32_t *query_order, const void *grad_out, void *grad_value,
+    void *grad_sampling_locations, void *grad_attention_weights, const msda_dims_t *dims,
+    msda_dtype_t dtype, void *stream);
+
 /* The integer parts every kernel uses, for bit-exact checks (same device
  * code as the forward and backward kernels). For each sample s (flattened
  * (b,q,m,l,k)) and corner c in order 00, 01, 10, 11, writes to the device

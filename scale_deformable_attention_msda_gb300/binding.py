@@ -23,7 +23,8 @@ STATUS = {0: "MSDA_OK", 1: "MSDA_ERR_NULL", 2: "MSDA_ERR_SHAPE", 3: "MSDA_ERR_DT
           4: "MSDA_ERR_ALIGN", 5: "MSDA_ERR_WORKSPACE", 6: "MSDA_ERR_CUDA"}
 EXPORTED = ("msda_forward", "msda_backward_workspace_bytes", "msda_backward",
             "msda_backward_zero", "msda_backward_accumulate", "msda_backward_finish",
-            "msda_debug_corners", "msda_status_string", "msda_version")
+            "msda_backward_static_workspace", "msda_debug_corners", "msda_status_string",
+            "msda_version")
 
 
 class msda_dims_t(ctypes.Structure):
@@ -68,6 +69,9 @@ def load(path: str | None = None):
     so.msda_backward_finish.argtypes = [vp, ctypes.c_size_t, vp, ctypes.c_int, dims, ctypes.c_int,
                                         vp]
     so.msda_backward_finish.restype = ctypes.c_int
+    so.msda_backward_static_workspace.argtypes = [vp, vp, vp, vp, vp, i32p, vp, vp, vp, vp, dims,
+                                                  ctypes.c_int, vp]
+    so.msda_backward_static_workspace.restype = ctypes.c_int
     so.msda_debug_corners.argtypes = [vp, vp, vp, vp, dims, ctypes.c_int, vp]
     so.msda_debug_corners.restype = ctypes.c_int
     so.msda_status_string.argtypes = [ctypes.c_int]
