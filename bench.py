@@ -38,6 +38,11 @@ METRIC = "MSDA fwd+bwd queries/sec at encoder scale; achieved HBM GB/s vs GB300 
 UNIT = "queries/s"
 FLUSH_BYTES = 256 << 20
 FALLBACK_HBM_GBS = 6800.0
+# L2 reduction throughput of this machine's GB300 for random 16-byte vector adds,
+# GB/s of reduction data, by bytes each group of lanes adds per instruction
+# (measured by scale_deformable_attention_msda_gb300/probes/memprobe.cu: the
+# 64 MiB footprint rows). The backward is bound by this, not by HBM.
+RED_CEILING_GBS = {64: 5902.0, 128: 7003.0}
 
 
 def parse_args(argv=None):
@@ -371,6 +376,20 @@ def run_ours(args):
             k.update(algorithmic_bytes=algo[n], gbs=round(gbs, 1), hbm_frac=round(gbs / peak, 4))
         kernels[n] = k
     step_bytes = cb["forward"] + cb["backward"]
+    # atomic bytes the backward adds into its accumulation target per launch
+    # (every corner of every sample, at the target's element size) and the
+    # group width of one vector add: 16 bytes per lane x lanes per group
+    acc_bytes = 4 if (args.dtype == "f32" or accum == binding.MSDA_ACC_FP32_BUFFER) else 2
+    red_bytes = w.samples * 4 * w.D * acc_bytes
+    lanes = w.D // (4 if args.dtype == "f32" else 8)
+    chunk = 16 * lanes
+    ceiling = RED_CEILING_GBS[128 if chunk >= 128 else 64]
+    red_gbs = red_bytes / (mean["backward"] * 1e-3) / 1e9
+    atomic_roofline = {"kernel": "msda_backward_kernel", "bound": "l2_reduction",
+                       "achieved": round(red_gbs, 1), "peak": ceiling, "unit": "GB/s",
+                       "frac": round(red_gbs / ceiling, 4), "atomic_bytes": red_bytes,
+                       "peak_source": "measured red.global.add.v4 throughput, "
+                                      f"{chunk}-byte groups (probes/memprobe.cu)"}
 
     result = None
     if rank == 0:
@@ -395,6 +414,7 @@ def run_ours(args):
                          "frac": round(step_bytes / (ms_per_step * 1e-3) / 1e9 / peak, 4)},
             "kernels": kernels,
             "roofline": roofline,
+            "atomic_roofline": atomic_roofline,
             "cpu_baseline": cpu,
             "e2e": e2e,
             "gpu_launches": launches_per_step * args.steps,

@@ -30,7 +30,7 @@ msda_forward_kernel(const Params p) {
     constexpr int GPW = 32 / LPG;            // groups per warp
     constexpr int SPW = 64;                  // descriptors per warp per chunk
     constexpr int CH = SPW / GPW;            // samples per group per chunk
-    constexpr int U = CH < 4 ? CH : 4;       // samples per gather step
+    constexpr int U = CH < 8 ? CH : 8;       // samples per gather step (8: 32 loads in flight)
 
     __shared__ LevelTable lt;
     __shared__ float4 s_w[kWarpsPerBlock][SPW];
