@@ -154,6 +154,30 @@ MSDA_API msda_status_t msda_backward(const void *value, const int64_t *spatial_s
                             const msda_dims_t *dims, msda_dtype_t dtype,
                             void *stream);
 
+/* The softmax variant: attention_logits (B, Q, M, L, K) are raw logits and
+ * the operator uses a = softmax over the L*K logits of each (b,q,m) -- the
+ * method the deformops README ("Multi-scale deformable attention") describes
+ * for normalising logits jointly over levels and points inside the kernel.
+ * msda_forward_softmax: as msda_forward with a in place of the weights.
+ * msda_backward_softmax: as msda_backward, writing d loss / d logit to
+ *   grad_attention_logits: a * (g_a - sum_j a_j g_a_j), g_a = d loss / d a.
+ * Logits must be finite. Supported: L*K <= 16 * D / (16 / element size), i.e.
+ * L*K <= 64 for 16-bit D = 32 and <= 128 for fp32 D = 32 (MSDA_ERR_SHAPE
+ * otherwise). Errors and alignment as msda_forward / msda_backward. */
+MSDA_API msda_status_t msda_forward_softmax(const void *value, const int64_t *spatial_shapes,
+                                            const int64_t *level_start_index,
+                                            const void *sampling_locations,
+                                            const void *attention_logits,
+                                            const int32_t *query_order, void *out,
+                                            const msda_dims_t *dims, msda_dtype_t dtype,
+                                            void *stream);
+MSDA_API msda_status_t msda_backward_softmax(
+    const void *value, const int64_t *spatial_shapes, const int64_t *level_start_index,
+    const void *sampling_locations, const void *attention_logits, const int32_t *query_order,
+    const void *grad_out, void *grad_value, void *grad_sampling_locations,
+    void *grad_attention_logits, void *workspace, size_t workspace_bytes, msda_accum_t accum,
+    const msda_dims_t *dims, msda_dtype_t dtype, void *stream);
+
 /* The same backward in three steps, for callers that sum grad_value over
  * several calls sharing one value tensor (or that time the kernels apart).
  * msda_backward(...) is exactly zero + accumulate + finish on one stream.

@@ -151,3 +151,37 @@ def corners(spatial_shapes, level_start_index, sampling_locations, lib=None):
     if rc != 0:
         raise ValueError("oracle corners rejected its arguments")
     return idx
+
+
+# --------------------------------------------------------------------------
+# The softmax variant (deformops README, "Multi-scale deformable attention":
+# with the softmax method the kernel normalises raw logits jointly over the
+# levels and points of each (b, q, m)). Composition of a softmax over the L*K
+# logits with the operator above; the backward is the chain rule through the
+# softmax: d loss / d z_i = a_i (g_i - sum_j a_j g_j) with g = d loss / d a.
+
+def softmax_weights(logits):
+    """a (B,Q,M,L,K) = softmax of the logits over their last two axes jointly."""
+    z = _f64(logits)
+    lead = z.shape[:-2]
+    flat = z.reshape(lead + (-1,))
+    e = np.exp(flat - flat.max(axis=-1, keepdims=True))
+    return (e / e.sum(axis=-1, keepdims=True)).reshape(z.shape)
+
+
+def forward_softmax(value, spatial_shapes, level_start_index, sampling_locations,
+                    attention_logits, nthreads: int = 0, lib=None):
+    return forward(value, spatial_shapes, level_start_index, sampling_locations,
+                   softmax_weights(attention_logits), nthreads=nthreads, lib=lib)
+
+
+def backward_softmax(value, spatial_shapes, level_start_index, sampling_locations,
+                     attention_logits, grad_out, nthreads: int = 0, lib=None):
+    """(grad_value, grad_loc, grad_logits), float64."""
+    a = softmax_weights(attention_logits)
+    gv, gl, ga = backward(value, spatial_shapes, level_start_index, sampling_locations, a,
+                          grad_out, nthreads=nthreads, lib=lib)
+    lead = a.shape[:-2]
+    af, gf = a.reshape(lead + (-1,)), ga.reshape(lead + (-1,))
+    gz = af * (gf - np.sum(af * gf, axis=-1, keepdims=True))
+    return gv, gl, gz.reshape(a.shape)

@@ -23,8 +23,8 @@ STATUS = {0: "MSDA_OK", 1: "MSDA_ERR_NULL", 2: "MSDA_ERR_SHAPE", 3: "MSDA_ERR_DT
           4: "MSDA_ERR_ALIGN", 5: "MSDA_ERR_WORKSPACE", 6: "MSDA_ERR_CUDA"}
 EXPORTED = ("msda_forward", "msda_backward_workspace_bytes", "msda_backward",
             "msda_backward_zero", "msda_backward_accumulate", "msda_backward_finish",
-            "msda_backward_static_workspace", "msda_debug_corners", "msda_status_string",
-            "msda_version")
+            "msda_backward_static_workspace", "msda_forward_softmax", "msda_backward_softmax",
+            "msda_debug_corners", "msda_status_string", "msda_version")
 
 
 class msda_dims_t(ctypes.Structure):
@@ -62,6 +62,10 @@ def load(path: str | None = None):
     so.msda_backward.argtypes = [vp, vp, vp, vp, vp, i32p, vp, vp, vp, vp, vp, ctypes.c_size_t,
                                  ctypes.c_int, dims, ctypes.c_int, vp]
     so.msda_backward.restype = ctypes.c_int
+    so.msda_forward_softmax.argtypes = so.msda_forward.argtypes
+    so.msda_forward_softmax.restype = ctypes.c_int
+    so.msda_backward_softmax.argtypes = so.msda_backward.argtypes
+    so.msda_backward_softmax.restype = ctypes.c_int
     so.msda_backward_accumulate.argtypes = so.msda_backward.argtypes
     so.msda_backward_accumulate.restype = ctypes.c_int
     so.msda_backward_zero.argtypes = [vp, vp, ctypes.c_size_t, ctypes.c_int, dims, ctypes.c_int, vp]
@@ -132,14 +136,16 @@ def _call(name, status):
 
 
 def msda_forward(value, spatial_shapes, level_start_index, sampling_locations,
-                 attention_weights, query_order=None, out=None, stream=None):
-    """out (B, Q, M*D) of value's dtype; see msda_forward in include/msda.h."""
+                 attention_weights, query_order=None, out=None, stream=None, softmax=False):
+    """out (B, Q, M*D) of value's dtype; see msda_forward in include/msda.h.
+    softmax=True: attention_weights are logits (msda_forward_softmax)."""
     d = dims_of(value, spatial_shapes, sampling_locations)
     if out is None:
         out = torch.empty((d.B, d.Q, d.M * d.D), dtype=value.dtype, device=value.device)
     _check_cuda(value, spatial_shapes, level_start_index, sampling_locations,
                 attention_weights, query_order, out)
-    _call("msda_forward", lib().msda_forward(
+    name = "msda_forward_softmax" if softmax else "msda_forward"
+    _call(name, getattr(lib(), name)(
         _ptr(value), _ptr(spatial_shapes), _ptr(level_start_index), _ptr(sampling_locations),
         _ptr(attention_weights), _ptr(query_order), _ptr(out), ctypes.byref(d), _dtype(value),
         _stream(stream)))
@@ -154,8 +160,10 @@ def msda_backward_workspace_bytes(dims: msda_dims_t, dtype, accum: int) -> int:
 def msda_backward(value, spatial_shapes, level_start_index, sampling_locations,
                   attention_weights, grad_out, accum: int = MSDA_ACC_FP32_BUFFER,
                   query_order=None, grad_value=None, grad_sampling_locations=None,
-                  grad_attention_weights=None, workspace=None, stream=None):
-    """(grad_value, grad_sampling_locations, grad_attention_weights)."""
+                  grad_attention_weights=None, workspace=None, stream=None, softmax=False):
+    """(grad_value, grad_sampling_locations, grad_attention_weights); with
+    softmax=True the weights are logits and the third output is their
+    gradient (msda_backward_softmax)."""
     d = dims_of(value, spatial_shapes, sampling_locations)
     dev, dt = value.device, value.dtype
     if grad_value is None:
@@ -171,7 +179,8 @@ def msda_backward(value, spatial_shapes, level_start_index, sampling_locations,
                 grad_out, query_order, grad_value, grad_sampling_locations,
                 grad_attention_weights, workspace)
     ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
-    _call("msda_backward", lib().msda_backward(
+    name = "msda_backward_softmax" if softmax else "msda_backward"
+    _call(name, getattr(lib(), name)(
         _ptr(value), _ptr(spatial_shapes), _ptr(level_start_index), _ptr(sampling_locations),
         _ptr(attention_weights), _ptr(query_order), _ptr(grad_out), _ptr(grad_value),
         _ptr(grad_sampling_locations), _ptr(grad_attention_weights), _ptr(workspace),

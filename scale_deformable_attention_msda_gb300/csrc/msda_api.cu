@@ -5,8 +5,9 @@
 #include "msda_common.cuh"
 
 namespace msda {
-cudaError_t launch_forward(const Params &p, msda_dtype_t dt, int lpg, cudaStream_t stream);
-cudaError_t launch_backward(const Params &p, msda_dtype_t dt, bool f32acc, int lpg,
+cudaError_t launch_forward(const Params &p, msda_dtype_t dt, int lpg, bool softmax,
+                           cudaStream_t stream);
+cudaError_t launch_backward(const Params &p, msda_dtype_t dt, bool f32acc, int lpg, bool softmax,
                             cudaStream_t stream);
 cudaError_t launch_zero(void *p, int64_t bytes, cudaStream_t stream);
 cudaError_t launch_convert(const float *ws, void *gv, int64_t n, msda_dtype_t dt,
@@ -71,6 +72,10 @@ Params make_params(const msda_dims_t &d) {
 
 msda_status_t from_cuda(cudaError_t e) { return e == cudaSuccess ? MSDA_OK : MSDA_ERR_CUDA; }
 
+// The softmax variant keeps d loss / d weight of a warp's query-heads in 512
+// fp32 shared-memory slots: L*K <= 512 / (32 / lanes per group).
+bool softmax_fits(const msda_dims_t &d, int lpg) { return d.L * d.K <= 16 * (int64_t)lpg; }
+
 // Pointers shared by the forward and the backward.
 msda_status_t check_common(const void *value, const int64_t *shapes, const int64_t *starts,
                            const void *loc, const void *attn, const msda_dims_t &d,
@@ -106,15 +111,16 @@ const char *msda_status_string(msda_status_t s) {
     return "unknown status";
 }
 
-msda_status_t msda_forward(const void *value, const int64_t *spatial_shapes,
-                           const int64_t *level_start_index, const void *sampling_locations,
-                           const void *attention_weights, const int32_t *query_order,
-                           void *out, const msda_dims_t *dims, msda_dtype_t dtype,
-                           void *stream) {
+static msda_status_t forward_impl(const void *value, const int64_t *spatial_shapes,
+                                  const int64_t *level_start_index,
+                                  const void *sampling_locations, const void *attention_weights,
+                                  const int32_t *query_order, void *out, const msda_dims_t *dims,
+                                  msda_dtype_t dtype, bool softmax, void *stream) {
     int lpg = 0;
     msda_status_t st = check_dims(dims, dtype, &lpg);
     if (st != MSDA_OK) return st;
     const msda_dims_t &d = *dims;
+    if (softmax && !softmax_fits(d, lpg)) return MSDA_ERR_SHAPE;
     st = check_common(value, spatial_shapes, level_start_index, sampling_locations,
                       attention_weights, d, dtype);
     if (st != MSDA_OK) return st;
@@ -129,7 +135,26 @@ msda_status_t msda_forward(const void *value, const int64_t *spatial_shapes,
     p.attn = attention_weights;
     p.order = query_order;
     p.out = out;
-    return from_cuda(msda::launch_forward(p, dtype, lpg, static_cast<cudaStream_t>(stream)));
+    return from_cuda(
+        msda::launch_forward(p, dtype, lpg, softmax, static_cast<cudaStream_t>(stream)));
+}
+
+msda_status_t msda_forward(const void *value, const int64_t *spatial_shapes,
+                           const int64_t *level_start_index, const void *sampling_locations,
+                           const void *attention_weights, const int32_t *query_order,
+                           void *out, const msda_dims_t *dims, msda_dtype_t dtype,
+                           void *stream) {
+    return forward_impl(value, spatial_shapes, level_start_index, sampling_locations,
+                        attention_weights, query_order, out, dims, dtype, false, stream);
+}
+
+msda_status_t msda_forward_softmax(const void *value, const int64_t *spatial_shapes,
+                                   const int64_t *level_start_index,
+                                   const void *sampling_locations, const void *attention_logits,
+                                   const int32_t *query_order, void *out,
+                                   const msda_dims_t *dims, msda_dtype_t dtype, void *stream) {
+    return forward_impl(value, spatial_shapes, level_start_index, sampling_locations,
+                        attention_logits, query_order, out, dims, dtype, true, stream);
 }
 
 size_t msda_backward_workspace_bytes(const msda_dims_t *dims, msda_dtype_t dtype,
@@ -184,20 +209,20 @@ msda_status_t msda_backward_zero(void *grad_value, void *workspace, size_t works
     return from_cuda(msda::launch_zero(bp.target, bp.target_bytes, static_cast<cudaStream_t>(stream)));
 }
 
-msda_status_t msda_backward_accumulate(const void *value, const int64_t *spatial_shapes,
-                                       const int64_t *level_start_index,
-                                       const void *sampling_locations,
-                                       const void *attention_weights,
-                                       const int32_t *query_order, const void *grad_out,
-                                       void *grad_value, void *grad_sampling_locations,
-                                       void *grad_attention_weights, void *workspace,
-                                       size_t workspace_bytes, msda_accum_t accum,
-                                       const msda_dims_t *dims, msda_dtype_t dtype,
-                                       void *stream) {
+static msda_status_t accumulate_impl(const void *value, const int64_t *spatial_shapes,
+                                     const int64_t *level_start_index,
+                                     const void *sampling_locations,
+                                     const void *attention_weights, const int32_t *query_order,
+                                     const void *grad_out, void *grad_value,
+                                     void *grad_sampling_locations, void *grad_attention_weights,
+                                     void *workspace, size_t workspace_bytes, msda_accum_t accum,
+                                     const msda_dims_t *dims, msda_dtype_t dtype, bool softmax,
+                                     void *stream) {
     BackwardPlan bp;
     msda_status_t st = plan_target(grad_value, workspace, workspace_bytes, accum, dims, dtype, &bp);
     if (st != MSDA_OK) return st;
     const msda_dims_t &d = *dims;
+    if (softmax && !softmax_fits(d, bp.lpg)) return MSDA_ERR_SHAPE;
     st = check_common(value, spatial_shapes, level_start_index, sampling_locations,
                       attention_weights, d, dtype);
     if (st != MSDA_OK) return st;
@@ -220,8 +245,24 @@ msda_status_t msda_backward_accumulate(const void *value, const int64_t *spatial
     p.grad_value = bp.target;
     p.grad_loc = grad_sampling_locations;
     p.grad_attn = grad_attention_weights;
-    return from_cuda(msda::launch_backward(p, dtype, bp.f32acc, bp.lpg,
+    return from_cuda(msda::launch_backward(p, dtype, bp.f32acc, bp.lpg, softmax,
                                            static_cast<cudaStream_t>(stream)));
+}
+
+msda_status_t msda_backward_accumulate(const void *value, const int64_t *spatial_shapes,
+                                       const int64_t *level_start_index,
+                                       const void *sampling_locations,
+                                       const void *attention_weights,
+                                       const int32_t *query_order, const void *grad_out,
+                                       void *grad_value, void *grad_sampling_locations,
+                                       void *grad_attention_weights, void *workspace,
+                                       size_t workspace_bytes, msda_accum_t accum,
+                                       const msda_dims_t *dims, msda_dtype_t dtype,
+                                       void *stream) {
+    return accumulate_impl(value, spatial_shapes, level_start_index, sampling_locations,
+                           attention_weights, query_order, grad_out, grad_value,
+                           grad_sampling_locations, grad_attention_weights, workspace,
+                           workspace_bytes, accum, dims, dtype, false, stream);
 }
 
 msda_status_t msda_backward_finish(const void *workspace, size_t workspace_bytes,
@@ -238,18 +279,21 @@ msda_status_t msda_backward_finish(const void *workspace, size_t workspace_bytes
                                           bp.nval, dtype, static_cast<cudaStream_t>(stream)));
 }
 
-msda_status_t msda_backward(const void *value, const int64_t *spatial_shapes,
-                            const int64_t *level_start_index, const void *sampling_locations,
-                            const void *attention_weights, const int32_t *query_order,
-                            const void *grad_out, void *grad_value,
-                            void *grad_sampling_locations, void *grad_attention_weights,
-                            void *workspace, size_t workspace_bytes, msda_accum_t accum,
-                            const msda_dims_t *dims, msda_dtype_t dtype, void *stream) {
+static msda_status_t backward_impl(const void *value, const int64_t *spatial_shapes,
+                                   const int64_t *level_start_index,
+                                   const void *sampling_locations, const void *attention_weights,
+                                   const int32_t *query_order, const void *grad_out,
+                                   void *grad_value, void *grad_sampling_locations,
+                                   void *grad_attention_weights, void *workspace,
+                                   size_t workspace_bytes, msda_accum_t accum,
+                                   const msda_dims_t *dims, msda_dtype_t dtype, bool softmax,
+                                   void *stream) {
     // Validate everything before the first launch, so that an error enqueues nothing.
     BackwardPlan bp;
     msda_status_t st = plan_target(grad_value, workspace, workspace_bytes, accum, dims, dtype, &bp);
     if (st != MSDA_OK) return st;
     const msda_dims_t &d = *dims;
+    if (softmax && !softmax_fits(d, bp.lpg)) return MSDA_ERR_SHAPE;
     st = check_common(value, spatial_shapes, level_start_index, sampling_locations,
                       attention_weights, d, dtype);
     if (st != MSDA_OK) return st;
@@ -265,12 +309,39 @@ msda_status_t msda_backward(const void *value, const int64_t *spatial_shapes,
         return MSDA_ERR_ALIGN;
     st = msda_backward_zero(grad_value, workspace, workspace_bytes, accum, dims, dtype, stream);
     if (st != MSDA_OK) return st;
-    st = msda_backward_accumulate(value, spatial_shapes, level_start_index, sampling_locations,
-                                  attention_weights, query_order, grad_out, grad_value,
-                                  grad_sampling_locations, grad_attention_weights, workspace,
-                                  workspace_bytes, accum, dims, dtype, stream);
+    st = accumulate_impl(value, spatial_shapes, level_start_index, sampling_locations,
+                         attention_weights, query_order, grad_out, grad_value,
+                         grad_sampling_locations, grad_attention_weights, workspace,
+                         workspace_bytes, accum, dims, dtype, softmax, stream);
     if (st != MSDA_OK) return st;
     return msda_backward_finish(workspace, workspace_bytes, grad_value, accum, dims, dtype, stream);
+}
+
+msda_status_t msda_backward(const void *value, const int64_t *spatial_shapes,
+                            const int64_t *level_start_index, const void *sampling_locations,
+                            const void *attention_weights, const int32_t *query_order,
+                            const void *grad_out, void *grad_value,
+                            void *grad_sampling_locations, void *grad_attention_weights,
+                            void *workspace, size_t workspace_bytes, msda_accum_t accum,
+                            const msda_dims_t *dims, msda_dtype_t dtype, void *stream) {
+    return backward_impl(value, spatial_shapes, level_start_index, sampling_locations,
+                         attention_weights, query_order, grad_out, grad_value,
+                         grad_sampling_locations, grad_attention_weights, workspace,
+                         workspace_bytes, accum, dims, dtype, false, stream);
+}
+
+msda_status_t msda_backward_softmax(const void *value, const int64_t *spatial_shapes,
+                                    const int64_t *level_start_index,
+                                    const void *sampling_locations, const void *attention_logits,
+                                    const int32_t *query_order, const void *grad_out,
+                                    void *grad_value, void *grad_sampling_locations,
+                                    void *grad_attention_logits, void *workspace,
+                                    size_t workspace_bytes, msda_accum_t accum,
+                                    const msda_dims_t *dims, msda_dtype_t dtype, void *stream) {
+    return backward_impl(value, spatial_shapes, level_start_index, sampling_locations,
+                         attention_logits, query_order, grad_out, grad_value,
+                         grad_sampling_locations, grad_attention_logits, workspace,
+                         workspace_bytes, accum, dims, dtype, true, stream);
 }
 
 msda_status_t msda_debug_corners(const int64_t *spatial_shapes, const int64_t *level_start_index,

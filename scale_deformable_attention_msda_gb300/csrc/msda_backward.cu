@@ -126,7 +126,12 @@ template <> __device__ __forceinline__ void store_xy<__half>(__half *p, float x,
     *reinterpret_cast<__half2 *>(p) = __floats2half2_rn(x, y);
 }
 
-template <typename T, int LPG, bool F32ACC>
+// Per-warp fp32 slots that hold d loss / d weight of every sample of the
+// warp's query-heads until the softmax backward can combine them: GPW
+// query-heads x at most kSoftmaxSlots / GPW samples each.
+constexpr int kSoftmaxSlots = 512;
+
+template <typename T, int LPG, bool F32ACC, bool SOFTMAX>
 __global__ void __launch_bounds__(kThreads)
 msda_backward_kernel(const Params p) {
     constexpr int VEC = Vec16<T>::N;
@@ -142,6 +147,8 @@ msda_backward_kernel(const Params p) {
     __shared__ float4 s_w[kWarpsPerBlock][SPW];
     __shared__ int4 s_o[kWarpsPerBlock][SPW];
     __shared__ float4 s_dot[kWarpsPerBlock][SPW];
+    __shared__ float s_ga[kWarpsPerBlock][SOFTMAX ? kSoftmaxSlots : 1];
+    constexpr int SLOTS = SOFTMAX ? kSoftmaxSlots / GPW : 1;   // samples per query-head
 
     load_level_table(lt, p);
     __syncthreads();
@@ -186,6 +193,12 @@ msda_backward_kernel(const Params p) {
     T *gloc = reinterpret_cast<T *>(p.grad_loc);
     T *gattn = reinterpret_cast<T *>(p.grad_attn);
 
+    // With SOFTMAX, attn holds logits and grad_attn receives d loss / d logit:
+    // a = softmax(logits), g_logit = a * (g_a - sum_j a_j g_a_j).
+    SoftmaxStats sm = {0.0f, 1.0f};
+    if (SOFTMAX) sm = softmax_stats<T, LPG>(attn + trp.bqm * p.LK, prep_ok ? p.LK : 0, lane);
+    float sum_ag = 0.0f;
+
     for (int base = 0; base < p.LK; base += CH) {
         // ---- phase 1: descriptors, and the finishing state of each sample
         float f_lx[NP], f_ly[NP], f_a[NP], f_W[NP], f_H[NP];
@@ -200,7 +213,8 @@ msda_backward_kernel(const Params p) {
             if (prep_ok && idx < p.LK) {
                 const int64_t e = trp.bqm * p.LK + idx;
                 const float2 xy = load_xy<T>(loc + 2 * e);
-                const float a = load_scalar<T>(attn + e);
+                const float a = SOFTMAX ? softmax_weight(load_scalar<T>(attn + e), sm)
+                                        : load_scalar<T>(attn + e);
                 const int l = level_of(idx, p.inv_K);
                 SampleGeom sg;
                 sample_geometry(sg, xy.x, xy.y, lt, l);
@@ -281,11 +295,30 @@ msda_backward_kernel(const Params p) {
                 const float dlx = hy * (s01 - s00) + ly * (s11 - s10);
                 const float dly = hx * (s10 - s00) + lx * (s11 - s01);
                 const int64_t e = trp.bqm * p.LK + idx;
-                gattn[e] = Elem<T>::from_f(ga);
+                if (SOFTMAX) {
+                    s_ga[warp][pg * SLOTS + idx] = ga;
+                    sum_ag += f_a[i] * ga;
+                } else {
+                    gattn[e] = Elem<T>::from_f(ga);
+                }
                 store_xy<T>(gloc + 2 * e, f_a[i] * f_W[i] * dlx, f_a[i] * f_H[i] * dly);
             }
         }
         __syncwarp();
+    }
+
+    if (SOFTMAX) {
+        // the lanes of one query-head differ in the lane bits above GPW
+#pragma unroll
+        for (int off = GPW; off < 32; off <<= 1) sum_ag += __shfl_xor_sync(0xffffffffu, sum_ag, off);
+        __syncwarp();
+        if (prep_ok) {
+            for (int idx = pj; idx < p.LK; idx += LPG) {
+                const int64_t e = trp.bqm * p.LK + idx;
+                const float a = softmax_weight(load_scalar<T>(attn + e), sm);
+                gattn[e] = Elem<T>::from_f(a * (s_ga[warp][pg * SLOTS + idx] - sum_ag));
+            }
+        }
     }
 }
 
@@ -335,7 +368,7 @@ cudaError_t launch_convert(const float *ws, void *gv, int64_t n, msda_dtype_t dt
     return cudaGetLastError();
 }
 
-template <typename T, bool F32ACC>
+template <typename T, bool F32ACC, bool SOFTMAX>
 static cudaError_t launch_backward_t(const Params &p, int lpg, cudaStream_t stream) {
     const int gpw = 32 / lpg;
     const int64_t warps = (p.triples + gpw - 1) / gpw;
@@ -344,29 +377,36 @@ static cudaError_t launch_backward_t(const Params &p, int lpg, cudaStream_t stre
     if (blocks > 0x7fffffff) return cudaErrorInvalidConfiguration;
     const dim3 grid((unsigned)blocks);
     switch (lpg) {
-        case 1: msda_backward_kernel<T, 1, F32ACC><<<grid, kThreads, 0, stream>>>(p); break;
-        case 2: msda_backward_kernel<T, 2, F32ACC><<<grid, kThreads, 0, stream>>>(p); break;
-        case 4: msda_backward_kernel<T, 4, F32ACC><<<grid, kThreads, 0, stream>>>(p); break;
-        case 8: msda_backward_kernel<T, 8, F32ACC><<<grid, kThreads, 0, stream>>>(p); break;
-        case 16: msda_backward_kernel<T, 16, F32ACC><<<grid, kThreads, 0, stream>>>(p); break;
-        case 32: msda_backward_kernel<T, 32, F32ACC><<<grid, kThreads, 0, stream>>>(p); break;
+        case 1: msda_backward_kernel<T, 1, F32ACC, SOFTMAX><<<grid, kThreads, 0, stream>>>(p); break;
+        case 2: msda_backward_kernel<T, 2, F32ACC, SOFTMAX><<<grid, kThreads, 0, stream>>>(p); break;
+        case 4: msda_backward_kernel<T, 4, F32ACC, SOFTMAX><<<grid, kThreads, 0, stream>>>(p); break;
+        case 8: msda_backward_kernel<T, 8, F32ACC, SOFTMAX><<<grid, kThreads, 0, stream>>>(p); break;
+        case 16: msda_backward_kernel<T, 16, F32ACC, SOFTMAX><<<grid, kThreads, 0, stream>>>(p); break;
+        case 32: msda_backward_kernel<T, 32, F32ACC, SOFTMAX><<<grid, kThreads, 0, stream>>>(p); break;
         default: return cudaErrorInvalidValue;
     }
     return cudaGetLastError();
 }
 
-cudaError_t launch_backward(const Params &p, msda_dtype_t dt, bool f32acc, int lpg,
-                            cudaStream_t stream) {
+template <bool SOFTMAX>
+static cudaError_t launch_backward_s(const Params &p, msda_dtype_t dt, bool f32acc, int lpg,
+                                     cudaStream_t stream) {
     switch (dt) {
-        case MSDA_F32: return launch_backward_t<float, true>(p, lpg, stream);
+        case MSDA_F32: return launch_backward_t<float, true, SOFTMAX>(p, lpg, stream);
         case MSDA_BF16:
-            return f32acc ? launch_backward_t<__nv_bfloat16, true>(p, lpg, stream)
-                          : launch_backward_t<__nv_bfloat16, false>(p, lpg, stream);
+            return f32acc ? launch_backward_t<__nv_bfloat16, true, SOFTMAX>(p, lpg, stream)
+                          : launch_backward_t<__nv_bfloat16, false, SOFTMAX>(p, lpg, stream);
         case MSDA_F16:
-            return f32acc ? launch_backward_t<__half, true>(p, lpg, stream)
-                          : launch_backward_t<__half, false>(p, lpg, stream);
+            return f32acc ? launch_backward_t<__half, true, SOFTMAX>(p, lpg, stream)
+                          : launch_backward_t<__half, false, SOFTMAX>(p, lpg, stream);
     }
     return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_backward(const Params &p, msda_dtype_t dt, bool f32acc, int lpg, bool softmax,
+                            cudaStream_t stream) {
+    return softmax ? launch_backward_s<true>(p, dt, f32acc, lpg, stream)
+                   : launch_backward_s<false>(p, dt, f32acc, lpg, stream);
 }
 
 }  // namespace msda

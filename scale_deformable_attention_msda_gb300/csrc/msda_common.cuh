@@ -228,6 +228,37 @@ __device__ __forceinline__ int level_of(int idx, float inv_K) {
     return (int)(((float)idx + 0.5f) * inv_K);
 }
 
+// Softmax over the L*K logits of one query-head, for the variant that takes
+// logits (deformops README, "Multi-scale deformable attention": the softmax
+// method normalises the logits jointly over levels and points). The lanes
+// that prepare one query-head are lane % GPW == const, so lane `lane` reads
+// logits pj, pj + LPG, ... (pj = lane / GPW) and the partial max and sum are
+// combined with xor shuffles over the lane bits above GPW.
+struct SoftmaxStats {
+    float max, inv_sum;
+};
+
+// Every lane of the warp must call this (it shuffles); a lane whose group has
+// no query passes LK = 0 and gets a value it does not use.
+template <typename T, int LPG>
+__device__ __forceinline__ SoftmaxStats softmax_stats(const T *logits, int LK, int lane) {
+    constexpr int GPW = 32 / LPG;
+    const int pj = lane / GPW;
+    float mx = -INFINITY;
+    for (int i = pj; i < LK; i += LPG) mx = fmaxf(mx, load_scalar<T>(logits + i));
+#pragma unroll
+    for (int off = GPW; off < 32; off <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+    float sum = 0.0f;
+    for (int i = pj; i < LK; i += LPG) sum += expf(load_scalar<T>(logits + i) - mx);
+#pragma unroll
+    for (int off = GPW; off < 32; off <<= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
+    return SoftmaxStats{mx, 1.0f / sum};
+}
+
+__device__ __forceinline__ float softmax_weight(float logit, const SoftmaxStats &s) {
+    return expf(logit - s.max) * s.inv_sum;
+}
+
 // (b, q, m) of triple t in dispatch order, and its linear (b*Q+q)*M+m index.
 struct Triple {
     int b, q, m;

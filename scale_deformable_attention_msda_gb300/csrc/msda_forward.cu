@@ -23,7 +23,7 @@
 
 namespace msda {
 
-template <typename T, int LPG>
+template <typename T, int LPG, bool SOFTMAX>
 __global__ void __launch_bounds__(kThreads)
 msda_forward_kernel(const Params p) {
     constexpr int VEC = Vec16<T>::N;
@@ -65,6 +65,11 @@ msda_forward_kernel(const Params p) {
     const T *loc = reinterpret_cast<const T *>(p.loc);
     const T *attn = reinterpret_cast<const T *>(p.attn);
 
+    // With SOFTMAX, attn holds logits: the weight of sample idx is
+    // exp(logit - max) / sum over the L*K logits of the prepared query-head.
+    SoftmaxStats sm = {0.0f, 1.0f};
+    if (SOFTMAX) sm = softmax_stats<T, LPG>(attn + trp.bqm * p.LK, prep_ok ? p.LK : 0, lane);
+
     float acc[VEC];
 #pragma unroll
     for (int i = 0; i < VEC; ++i) acc[i] = 0.0f;
@@ -80,7 +85,8 @@ msda_forward_kernel(const Params p) {
             if (prep_ok && idx < p.LK) {
                 const int64_t e = trp.bqm * p.LK + idx;
                 const float2 xy = load_xy<T>(loc + 2 * e);
-                const float a = load_scalar<T>(attn + e);
+                const float a = SOFTMAX ? softmax_weight(load_scalar<T>(attn + e), sm)
+                                        : load_scalar<T>(attn + e);
                 const int l = level_of(idx, p.inv_K);
                 SampleGeom sg;
                 sample_geometry(sg, xy.x, xy.y, lt, l);
@@ -129,7 +135,7 @@ msda_forward_kernel(const Params p) {
     }
 }
 
-template <typename T>
+template <typename T, bool SOFTMAX>
 static cudaError_t launch_forward_t(const Params &p, int lpg, cudaStream_t stream) {
     const int gpw = 32 / lpg;
     const int64_t warps = (p.triples + gpw - 1) / gpw;
@@ -138,22 +144,29 @@ static cudaError_t launch_forward_t(const Params &p, int lpg, cudaStream_t strea
     if (blocks > 0x7fffffff) return cudaErrorInvalidConfiguration;
     const dim3 grid((unsigned)blocks);
     switch (lpg) {
-        case 1: msda_forward_kernel<T, 1><<<grid, kThreads, 0, stream>>>(p); break;
-        case 2: msda_forward_kernel<T, 2><<<grid, kThreads, 0, stream>>>(p); break;
-        case 4: msda_forward_kernel<T, 4><<<grid, kThreads, 0, stream>>>(p); break;
-        case 8: msda_forward_kernel<T, 8><<<grid, kThreads, 0, stream>>>(p); break;
-        case 16: msda_forward_kernel<T, 16><<<grid, kThreads, 0, stream>>>(p); break;
-        case 32: msda_forward_kernel<T, 32><<<grid, kThreads, 0, stream>>>(p); break;
+        case 1: msda_forward_kernel<T, 1, SOFTMAX><<<grid, kThreads, 0, stream>>>(p); break;
+        case 2: msda_forward_kernel<T, 2, SOFTMAX><<<grid, kThreads, 0, stream>>>(p); break;
+        case 4: msda_forward_kernel<T, 4, SOFTMAX><<<grid, kThreads, 0, stream>>>(p); break;
+        case 8: msda_forward_kernel<T, 8, SOFTMAX><<<grid, kThreads, 0, stream>>>(p); break;
+        case 16: msda_forward_kernel<T, 16, SOFTMAX><<<grid, kThreads, 0, stream>>>(p); break;
+        case 32: msda_forward_kernel<T, 32, SOFTMAX><<<grid, kThreads, 0, stream>>>(p); break;
         default: return cudaErrorInvalidValue;
     }
     return cudaGetLastError();
 }
 
-cudaError_t launch_forward(const Params &p, msda_dtype_t dt, int lpg, cudaStream_t stream) {
+cudaError_t launch_forward(const Params &p, msda_dtype_t dt, int lpg, bool softmax,
+                           cudaStream_t stream) {
     switch (dt) {
-        case MSDA_F32: return launch_forward_t<float>(p, lpg, stream);
-        case MSDA_BF16: return launch_forward_t<__nv_bfloat16>(p, lpg, stream);
-        case MSDA_F16: return launch_forward_t<__half>(p, lpg, stream);
+        case MSDA_F32:
+            return softmax ? launch_forward_t<float, true>(p, lpg, stream)
+                           : launch_forward_t<float, false>(p, lpg, stream);
+        case MSDA_BF16:
+            return softmax ? launch_forward_t<__nv_bfloat16, true>(p, lpg, stream)
+                           : launch_forward_t<__nv_bfloat16, false>(p, lpg, stream);
+        case MSDA_F16:
+            return softmax ? launch_forward_t<__half, true>(p, lpg, stream)
+                           : launch_forward_t<__half, false>(p, lpg, stream);
     }
     return cudaErrorInvalidValue;
 }

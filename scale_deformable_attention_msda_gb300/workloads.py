@@ -138,8 +138,8 @@ def make_inputs(wl: Workload, with_grad: bool = True) -> dict:
     """Draw every operand of one forward+backward call.
 
     Returns float64 arrays already on the dtype's grid: value (B,S,M,D),
-    loc (B,Q,M,L,K,2), attn (B,Q,M,L,K), grad_out (B,Q,M*D); int64
-    shapes (L,2) and starts (L,).
+    loc (B,Q,M,L,K,2), attn (B,Q,M,L,K) (softmax of logits), logits
+    (B,Q,M,L,K), grad_out (B,Q,M*D); int64 shapes (L,2) and starts (L,).
     """
     rng = np.random.Generator(np.random.PCG64(wl.seed))
     B, Q, M, D, L, K, S = wl.B, wl.Q, wl.M, wl.D, wl.L, wl.K, wl.S
@@ -166,6 +166,8 @@ def make_inputs(wl: Workload, with_grad: bool = True) -> dict:
         "starts": level_start_index(wl.levels),
         "loc": round_to(loc, wl.dtype),
         "attn": round_to(attn, wl.dtype),
+        # the raw logits, for the variant that applies the softmax itself
+        "logits": round_to(logits.reshape(B, Q, M, L, K), wl.dtype),
     }
     if with_grad:
         out["grad_out"] = round_to(rng.standard_normal((B, Q, M * D)), wl.dtype)

@@ -170,6 +170,28 @@ def test_dispatch_order_changes_nothing(kind):
     check(got, oracle_run(p), w.dtype, f"order {kind}")
 
 
+# ------------------------------------------------ the softmax variant
+
+@pytest.mark.parametrize("w", [wl.tiny(), wl.decoder("f32"), wl.decoder("bf16"),
+                               wl.encoder("f32"), wl.encoder("bf16"),
+                               wl.sweep(5000, 8, 4)],
+                         ids=lambda w: f"{w.name}-{w.dtype}")
+def test_softmax_variant(w):
+    p = wl.make_inputs(w)
+    t = upload(p, w.dtype)
+    z = to_dev(p["logits"], w.dtype)
+    out = binding.msda_forward(t["value"], t["shapes"], t["starts"], t["loc"], z, softmax=True)
+    gv, gl, gz = binding.msda_backward(t["value"], t["shapes"], t["starts"], t["loc"], z,
+                                       t["grad_out"], softmax=True)
+    torch.cuda.synchronize()
+    got = {"out": np64(out), "gv": np64(gv), "gl": np64(gl), "ga": np64(gz)}
+    ref = {"out": oracle.forward_softmax(p["value"], p["shapes"], p["starts"], p["loc"],
+                                         p["logits"])}
+    ref["gv"], ref["gl"], ref["ga"] = oracle.backward_softmax(
+        p["value"], p["shapes"], p["starts"], p["loc"], p["logits"], p["grad_out"])
+    check(got, ref, w.dtype, f"softmax {w.name}")
+
+
 # ------------------------------------------------------- integer parity
 
 def _corners_case(w, loc=None):

@@ -108,6 +108,17 @@ def test_validation_errors_before_any_launch(so):
     assert _fwd(so, _dims(), order=FAKE + 2) == 4
 
 
+def test_softmax_variant_size_limit(so):
+    vp = ctypes.c_void_p
+    # bf16, D = 32: 4 lanes per query-head, so at most 64 samples per query-head
+    ok = _dims(L=4, K=16, Q=0)            # 64 samples, empty: valid, launches nothing
+    big = _dims(L=4, K=17)                # 68 samples: refused before any launch
+    args = lambda d: (vp(FAKE), vp(FAKE), vp(FAKE), vp(FAKE), vp(FAKE), vp(None), vp(FAKE),
+                      ctypes.byref(d), 1, vp(0))
+    assert so.msda_forward_softmax(*args(ok)) == 0
+    assert so.msda_forward_softmax(*args(big)) == 2
+
+
 def test_empty_problems_are_valid_and_launch_nothing(so):
     assert _fwd(so, _dims(B=0)) == 0
     assert _fwd(so, _dims(Q=0)) == 0

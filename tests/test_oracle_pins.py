@@ -435,3 +435,61 @@ def test_pins_catch_planted_mistake(oracle_mod, name):
         lib = oracle_mod.compile_library(path, os.path.join(d, "m.so"))
         failed = _run_checks_in_child(lib)
     assert failed, f"no pin caught mutation {name}"
+
+
+# ------------------------------------------------ the softmax variant
+
+def test_softmax_variant_constant_map(oracle_mod):
+    """Softmax weights sum to 1: interior samples of a constant map return it."""
+    w = wl.Workload("c", B=1, Q=20, M=3, D=2, K=3, levels=((10, 12), (5, 6)), sigma_px=0.5,
+                    seed=6)
+    p = wl.make_inputs(w)
+    loc = p["loc"].copy()
+    for l, (h, ww) in enumerate(w.levels):
+        loc[..., l, :, 0] = np.clip(loc[..., l, :, 0], 1.0 / ww, 1 - 1.0 / ww)
+        loc[..., l, :, 1] = np.clip(loc[..., l, :, 1], 1.0 / h, 1 - 1.0 / h)
+    logits = np.random.default_rng(1).standard_normal(p["attn"].shape) * 3
+    out = oracle_mod.forward_softmax(np.full_like(p["value"], -1.5), p["shapes"], p["starts"],
+                                     loc, logits)
+    assert np.allclose(out, -1.5, rtol=0, atol=1e-14)
+
+
+def test_softmax_variant_matches_torch_autograd(oracle_mod):
+    p = _problem(B=2, Q=6, M=2, D=3, K=3, levels=((5, 7), (3, 4)), sigma=2.0, seed=17)
+    logits = np.random.default_rng(2).standard_normal(p["attn"].shape) * 2
+    t = {k: torch.tensor(v, dtype=torch.float64, requires_grad=True)
+         for k, v in (("value", p["value"]), ("loc", p["loc"]), ("z", logits))}
+    B, Q, M, L, K = logits.shape
+    a = torch.softmax(t["z"].reshape(B, Q, M, L * K), dim=-1).reshape(B, Q, M, L, K)
+    out = grid_sample_msda(t["value"], p["shapes"], p["starts"], t["loc"], a)
+    out.backward(torch.tensor(p["grad_out"]))
+    got = oracle_mod.forward_softmax(p["value"], p["shapes"], p["starts"], p["loc"], logits)
+    assert np.allclose(got, out.detach().numpy(), rtol=1e-12, atol=1e-12)
+    gv, gl, gz = oracle_mod.backward_softmax(p["value"], p["shapes"], p["starts"], p["loc"],
+                                             logits, p["grad_out"])
+    assert np.allclose(gv, t["value"].grad.numpy(), rtol=1e-11, atol=1e-11)
+    assert np.allclose(gz, t["z"].grad.numpy(), rtol=1e-11, atol=1e-11)
+    ok = _away_from_kinks(p, 1e-6)[..., None]
+    assert np.allclose(np.where(ok, gl, 0), np.where(ok, t["loc"].grad.numpy(), 0),
+                       rtol=1e-10, atol=1e-10)
+
+
+def test_softmax_variant_finite_differences(oracle_mod):
+    p = wl.make_inputs(wl.tiny())
+    logits = np.random.default_rng(3).standard_normal(p["attn"].shape)
+    g = p["grad_out"]
+    _, _, gz = oracle_mod.backward_softmax(p["value"], p["shapes"], p["starts"], p["loc"],
+                                           logits, g)
+    h = 1e-6
+    flat = logits.reshape(-1)
+    fd = np.empty(flat.size)
+    for i in range(flat.size):
+        zp, zm = flat.copy(), flat.copy()
+        zp[i] += h
+        zm[i] -= h
+        fp = np.sum(g * oracle_mod.forward_softmax(p["value"], p["shapes"], p["starts"], p["loc"],
+                                                   zp.reshape(logits.shape)))
+        fm = np.sum(g * oracle_mod.forward_softmax(p["value"], p["shapes"], p["starts"], p["loc"],
+                                                   zm.reshape(logits.shape)))
+        fd[i] = (fp - fm) / (2 * h)
+    assert np.linalg.norm(fd - gz.reshape(-1)) <= 1e-6 * np.linalg.norm(fd)
