@@ -41,8 +41,10 @@
  * A level whose table entry is not a non-empty rectangle inside [0, S)
  * (H_l < 1, W_l < 1, start < 0 or start + H_l*W_l > S) is treated as empty.
  *
- * Arithmetic: products and sums in fp32 for every storage dtype; a 16-bit
- * result is rounded once, to nearest even, when it is stored.
+ * Arithmetic: products and sums in fp32 for fp32 and 16-bit storage (a 16-bit
+ * result is rounded once, to nearest even, when it is stored); in fp64 for
+ * MSDA_F64, whose integer parts follow x = loc*W - 0.5 computed with a
+ * rounded multiply and a rounded add in double.
  */
 #ifndef MSDA_H
 #define MSDA_H
@@ -64,15 +66,16 @@ extern "C" {
 typedef enum {
     MSDA_F32 = 0,
     MSDA_BF16 = 1,
-    MSDA_F16 = 2
+    MSDA_F16 = 2,
+    MSDA_F64 = 3   /* double throughout: geometry, arithmetic and atomics */
 } msda_dtype_t;
 
 /* How msda_backward accumulates grad_value for a 16-bit dtype.
  * NATIVE: vector atomic adds straight into the 16-bit grad_value (each add
  *   rounds to the 16-bit format, so the result depends on contention).
  * FP32_BUFFER: atomic adds into a caller-provided fp32 workspace, then one
- *   rounding pass into grad_value. For MSDA_F32 both modes are the same
- *   (fp32 atomics into grad_value) and no workspace is needed.
+ *   rounding pass into grad_value. For MSDA_F32 and MSDA_F64 both modes are
+ *   the same (atomics of that type into grad_value) and no workspace is needed.
  * The pages motivate the switch: the Efficient-MSDA summary page, section
  * "The backward pass is an atomics problem", and the deformops README,
  * section "Backend selection" (fp32 accumulator vs native half atomics). */
@@ -94,7 +97,8 @@ typedef enum {
 /* Problem sizes. Supported: B >= 0, Q >= 0 (zero is a valid empty call),
  * S >= 1, M >= 1, 1 <= L <= 16, K >= 1, S*M*D < 2^31, and D a power-of-two
  * multiple of the 16-byte vector width: D/4 in {1,2,4,...,32} for MSDA_F32,
- * D/8 in {1,2,4,...,32} for 16-bit dtypes (D = 32 is the detector case). */
+ * D/8 in {1,2,4,...,32} for 16-bit dtypes, D/2 in {1,2,4,...,32} for
+ * MSDA_F64 (D = 32 is the detector case). */
 typedef struct {
     int64_t B, S, Q, M, D, L, K;
 } msda_dims_t;

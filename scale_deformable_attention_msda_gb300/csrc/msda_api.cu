@@ -13,14 +13,20 @@ cudaError_t launch_zero(void *p, int64_t bytes, cudaStream_t stream);
 cudaError_t launch_convert(const float *ws, void *gv, int64_t n, msda_dtype_t dt,
                            cudaStream_t stream);
 cudaError_t launch_corners(const Params &p, msda_dtype_t dt, int32_t *rows, cudaStream_t stream);
+cudaError_t launch_forward_f64(const Params &p, int lpg, bool softmax, cudaStream_t stream);
+cudaError_t launch_backward_f64(const Params &p, int lpg, bool softmax, cudaStream_t stream);
+cudaError_t launch_corners_f64(const Params &p, int32_t *rows, cudaStream_t stream);
 }  // namespace msda
 
 namespace {
 
 using msda::Params;
 
-bool dtype_ok(msda_dtype_t dt) { return dt == MSDA_F32 || dt == MSDA_BF16 || dt == MSDA_F16; }
-int elem_bytes(msda_dtype_t dt) { return dt == MSDA_F32 ? 4 : 2; }
+bool dtype_ok(msda_dtype_t dt) {
+    return dt == MSDA_F32 || dt == MSDA_BF16 || dt == MSDA_F16 || dt == MSDA_F64;
+}
+bool is_16bit(msda_dtype_t dt) { return dt == MSDA_BF16 || dt == MSDA_F16; }
+int elem_bytes(msda_dtype_t dt) { return dt == MSDA_F64 ? 8 : (dt == MSDA_F32 ? 4 : 2); }
 bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
 // Lanes per (b,q,m) group: D / (channels per 16 bytes), a power of two <= 32.
@@ -74,7 +80,9 @@ msda_status_t from_cuda(cudaError_t e) { return e == cudaSuccess ? MSDA_OK : MSD
 
 // The softmax variant keeps d loss / d weight of a warp's query-heads in 512
 // fp32 shared-memory slots: L*K <= 512 / (32 / lanes per group).
-bool softmax_fits(const msda_dims_t &d, int lpg) { return d.L * d.K <= 16 * (int64_t)lpg; }
+bool softmax_fits(const msda_dims_t &d, msda_dtype_t dt, int lpg) {
+    return dt == MSDA_F64 || d.L * d.K <= 16 * (int64_t)lpg;   // fp64 keeps no slots
+}
 
 // Pointers shared by the forward and the backward.
 msda_status_t check_common(const void *value, const int64_t *shapes, const int64_t *starts,
@@ -120,7 +128,7 @@ static msda_status_t forward_impl(const void *value, const int64_t *spatial_shap
     msda_status_t st = check_dims(dims, dtype, &lpg);
     if (st != MSDA_OK) return st;
     const msda_dims_t &d = *dims;
-    if (softmax && !softmax_fits(d, lpg)) return MSDA_ERR_SHAPE;
+    if (softmax && !softmax_fits(d, dtype, lpg)) return MSDA_ERR_SHAPE;
     st = check_common(value, spatial_shapes, level_start_index, sampling_locations,
                       attention_weights, d, dtype);
     if (st != MSDA_OK) return st;
@@ -135,8 +143,9 @@ static msda_status_t forward_impl(const void *value, const int64_t *spatial_shap
     p.attn = attention_weights;
     p.order = query_order;
     p.out = out;
-    return from_cuda(
-        msda::launch_forward(p, dtype, lpg, softmax, static_cast<cudaStream_t>(stream)));
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    return from_cuda(dtype == MSDA_F64 ? msda::launch_forward_f64(p, lpg, softmax, s)
+                                       : msda::launch_forward(p, dtype, lpg, softmax, s));
 }
 
 msda_status_t msda_forward(const void *value, const int64_t *spatial_shapes,
@@ -160,7 +169,7 @@ msda_status_t msda_forward_softmax(const void *value, const int64_t *spatial_sha
 size_t msda_backward_workspace_bytes(const msda_dims_t *dims, msda_dtype_t dtype,
                                      msda_accum_t accum) {
     if (check_dims(dims, dtype, nullptr) != MSDA_OK) return 0;
-    if (dtype == MSDA_F32 || accum != MSDA_ACC_FP32_BUFFER) return 0;
+    if (!is_16bit(dtype) || accum != MSDA_ACC_FP32_BUFFER) return 0;
     return (size_t)(dims->B * dims->S * dims->M * dims->D) * sizeof(float);
 }
 
@@ -182,7 +191,7 @@ msda_status_t plan_target(void *grad_value, void *workspace, size_t workspace_by
     if (st != MSDA_OK) return st;
     if (accum != MSDA_ACC_NATIVE && accum != MSDA_ACC_FP32_BUFFER) return MSDA_ERR_DTYPE;
     const msda_dims_t &d = *dims;
-    bp->f32acc = dtype != MSDA_F32 && accum == MSDA_ACC_FP32_BUFFER;
+    bp->f32acc = is_16bit(dtype) && accum == MSDA_ACC_FP32_BUFFER;
     bp->nval = d.B * d.S * d.M * d.D;
     bp->target = bp->f32acc ? workspace : grad_value;
     bp->target_bytes = bp->nval * (bp->f32acc ? 4 : elem_bytes(dtype));
@@ -222,7 +231,7 @@ static msda_status_t accumulate_impl(const void *value, const int64_t *spatial_s
     msda_status_t st = plan_target(grad_value, workspace, workspace_bytes, accum, dims, dtype, &bp);
     if (st != MSDA_OK) return st;
     const msda_dims_t &d = *dims;
-    if (softmax && !softmax_fits(d, bp.lpg)) return MSDA_ERR_SHAPE;
+    if (softmax && !softmax_fits(d, dtype, bp.lpg)) return MSDA_ERR_SHAPE;
     st = check_common(value, spatial_shapes, level_start_index, sampling_locations,
                       attention_weights, d, dtype);
     if (st != MSDA_OK) return st;
@@ -245,8 +254,10 @@ static msda_status_t accumulate_impl(const void *value, const int64_t *spatial_s
     p.grad_value = bp.target;
     p.grad_loc = grad_sampling_locations;
     p.grad_attn = grad_attention_weights;
-    return from_cuda(msda::launch_backward(p, dtype, bp.f32acc, bp.lpg, softmax,
-                                           static_cast<cudaStream_t>(stream)));
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    return from_cuda(dtype == MSDA_F64
+                         ? msda::launch_backward_f64(p, bp.lpg, softmax, s)
+                         : msda::launch_backward(p, dtype, bp.f32acc, bp.lpg, softmax, s));
 }
 
 msda_status_t msda_backward_accumulate(const void *value, const int64_t *spatial_shapes,
@@ -293,7 +304,7 @@ static msda_status_t backward_impl(const void *value, const int64_t *spatial_sha
     msda_status_t st = plan_target(grad_value, workspace, workspace_bytes, accum, dims, dtype, &bp);
     if (st != MSDA_OK) return st;
     const msda_dims_t &d = *dims;
-    if (softmax && !softmax_fits(d, bp.lpg)) return MSDA_ERR_SHAPE;
+    if (softmax && !softmax_fits(d, dtype, bp.lpg)) return MSDA_ERR_SHAPE;
     st = check_common(value, spatial_shapes, level_start_index, sampling_locations,
                       attention_weights, d, dtype);
     if (st != MSDA_OK) return st;
@@ -373,7 +384,9 @@ msda_status_t msda_debug_corners(const int64_t *spatial_shapes, const int64_t *l
     p.LK = (int)(d.L * d.K);
     p.inv_K = 1.0f / (float)d.K;
     p.triples = d.B * d.Q * d.M;
-    return from_cuda(msda::launch_corners(p, dtype, corner_rows, static_cast<cudaStream_t>(stream)));
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    return from_cuda(dtype == MSDA_F64 ? msda::launch_corners_f64(p, corner_rows, s)
+                                       : msda::launch_corners(p, dtype, corner_rows, s));
 }
 
 }  // extern "C"

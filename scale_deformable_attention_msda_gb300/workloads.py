@@ -38,7 +38,7 @@ LEVELS_DETR = ((100, 167), (50, 84), (25, 42), (13, 21))   # strides 8..64 of 80
 LEVELS_M2F = ((128, 128), (64, 64), (32, 32))              # strides 8..32 of 1024^2
 LEVELS_TINY = ((8, 8), (4, 4))
 
-DTYPES = ("f32", "bf16", "f16")
+DTYPES = ("f32", "bf16", "f16", "f64")
 
 
 @dataclass(frozen=True)
@@ -88,6 +88,8 @@ def spatial_shapes(levels) -> np.ndarray:
 
 def round_to(x: np.ndarray, dtype: str) -> np.ndarray:
     x = np.asarray(x, dtype=np.float64)
+    if dtype == "f64":
+        return x.copy()
     if dtype == "f32":
         return x.astype(np.float32).astype(np.float64)
     if dtype == "f16":
@@ -279,7 +281,7 @@ def sweep_grid():
 # --------------------------------------------------------------------------
 # counting (for the benchmark's roofline; no operator arithmetic)
 
-ELEMENT_BYTES = {"f32": 4, "bf16": 2, "f16": 2}
+ELEMENT_BYTES = {"f64": 8, "f32": 4, "bf16": 2, "f16": 2}
 
 
 def compulsory_bytes(wl: Workload) -> dict:

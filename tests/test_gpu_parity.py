@@ -4,6 +4,8 @@ Tolerances:
   fp32 forward      max |gpu - oracle| <= 1e-5 * max |oracle|
   fp32 backward     relative L2 error <= 1e-4 for each gradient
   bf16 / fp16       relative L2 error <= 2e-2 (forward and backward)
+  fp64              forward max error <= 1e-12 * max |oracle|, gradients
+                    relative L2 <= 1e-12 (only the summation order differs)
   integer parts     bit-exact (corner rows and in-map masks)
 The oracle receives exactly the values the GPU saw (16-bit inputs upcast).
 Every workload runs at its full size; the oracle finishes each in seconds.
@@ -17,7 +19,8 @@ from scale_deformable_attention_msda_gb300 import binding, workloads as wl
 
 pytestmark = pytest.mark.gpu
 
-TORCH_DTYPE = {"f32": torch.float32, "bf16": torch.bfloat16, "f16": torch.float16}
+TORCH_DTYPE = {"f32": torch.float32, "bf16": torch.bfloat16, "f16": torch.float16,
+               "f64": torch.float64}
 NATIVE, FP32BUF = binding.MSDA_ACC_NATIVE, binding.MSDA_ACC_FP32_BUFFER
 
 
@@ -78,14 +81,15 @@ def oracle_run(p, backward=True):
 
 def check(got, ref, dtype, label=""):
     errs = {}
-    if dtype == "f32":
+    if dtype in ("f32", "f64"):
+        tol_out, tol_grad = (1e-5, 1e-4) if dtype == "f32" else (1e-12, 1e-12)
         scale = max(np.max(np.abs(ref["out"])), 1e-300)
         errs["out"] = float(np.max(np.abs(got["out"] - ref["out"])) / scale)
-        assert errs["out"] <= 1e-5, (label, errs)
+        assert errs["out"] <= tol_out, (label, errs)
         for k in ("gv", "gl", "ga"):
             if k in got:
                 errs[k] = rel_l2(got[k], ref[k])
-                assert errs[k] <= 1e-4, (label, k, errs)
+                assert errs[k] <= tol_grad, (label, k, errs)
     else:
         for k in ("out", "gv", "gl", "ga"):
             if k in got:
@@ -151,6 +155,12 @@ def test_sweep_points(Q, K, L):
     run_and_check(wl.sweep(Q, K, L), FP32BUF)
 
 
+@pytest.mark.parametrize("w", [wl.tiny().with_dtype("f64"), wl.decoder("f64"), wl.encoder("f64")],
+                         ids=lambda w: w.name)
+def test_f64(w):
+    run_and_check(w)
+
+
 def test_sweep_contention():
     run_and_check(wl.sweep(5000, 4, 4, contention=True), FP32BUF)
 
@@ -174,7 +184,7 @@ def test_dispatch_order_changes_nothing(kind):
 
 @pytest.mark.parametrize("w", [wl.tiny(), wl.decoder("f32"), wl.decoder("bf16"),
                                wl.encoder("f32"), wl.encoder("bf16"),
-                               wl.sweep(5000, 8, 4)],
+                               wl.sweep(5000, 8, 4), wl.decoder("f64")],
                          ids=lambda w: f"{w.name}-{w.dtype}")
 def test_softmax_variant(w):
     p = wl.make_inputs(w)
@@ -207,20 +217,20 @@ def _corners_case(w, loc=None):
 
 @pytest.mark.parametrize("w", [wl.tiny(), wl.decoder("f32"), wl.decoder("bf16"),
                                wl.encoder("bf16"), wl.mask2former("bf16"),
-                               wl.sweep(5000, 4, 4, contention=True)],
+                               wl.sweep(5000, 4, 4, contention=True), wl.decoder("f64")],
                          ids=lambda w: f"{w.name}-{w.dtype}")
 def test_corner_rows_bit_exact(w):
     _corners_case(w)
 
 
-@pytest.mark.parametrize("dtype", ["f32", "bf16", "f16"])
+@pytest.mark.parametrize("dtype", ["f32", "bf16", "f16", "f64"])
 def test_corner_rows_at_cell_boundaries(dtype):
     """Locations whose pixel coordinate is an integer or one ulp either side:
     the floor must be the exact one on both sides."""
     levels = ((100, 167), (13, 21), (1, 1), (1, 5))
     w = wl.Workload("edges", B=1, Q=64, M=2, D=8, K=8, levels=levels, dtype=dtype, seed=9)
     rng = np.random.default_rng(1)
-    np_t = {"f32": np.float32, "f16": np.float16, "bf16": np.float32}[dtype]
+    np_t = {"f32": np.float32, "f16": np.float16, "bf16": np.float32, "f64": np.float64}[dtype]
     loc = np.empty((1, w.Q, w.M, w.L, w.K, 2))
     for l, (h, ww) in enumerate(levels):
         for axis, n in ((0, ww), (1, h)):
@@ -244,7 +254,7 @@ def _small(B=2, Q=37, M=3, D=8, K=3, levels=((9, 11), (4, 7), (1, 3)), dtype="f3
 
 @pytest.mark.parametrize("dtype,D", [("f32", 4), ("f32", 8), ("f32", 16), ("f32", 64),
                                      ("f32", 128), ("bf16", 8), ("bf16", 16), ("bf16", 64),
-                                     ("bf16", 256), ("f16", 32)])
+                                     ("bf16", 256), ("f16", 32), ("f64", 2), ("f64", 64)])
 def test_channel_widths(dtype, D):
     run_and_check(_small(D=D, dtype=dtype, M=2), FP32BUF, label=f"D={D}")
 
