@@ -246,31 +246,34 @@ def msda_debug_corners(spatial_shapes, level_start_index, sampling_locations, S:
 
 
 class MSDAFunction(torch.autograd.Function):
-    """Autograd wrapper: forward and backward both run libmsda kernels."""
+    """Autograd wrapper: forward and backward both run libmsda kernels.
+    With softmax=True the weights are logits (the fused-softmax variant)."""
 
     @staticmethod
     def forward(ctx, value, spatial_shapes, level_start_index, sampling_locations,
-                attention_weights, accum=MSDA_ACC_FP32_BUFFER):
+                attention_weights, accum=MSDA_ACC_FP32_BUFFER, softmax=False):
         ctx.save_for_backward(value, spatial_shapes, level_start_index, sampling_locations,
                               attention_weights)
         ctx.accum = accum
+        ctx.softmax = softmax
         return msda_forward(value, spatial_shapes, level_start_index, sampling_locations,
-                            attention_weights.contiguous())
+                            attention_weights, softmax=softmax)
 
     @staticmethod
     def backward(ctx, grad_out):
         value, shapes, starts, loc, attn = ctx.saved_tensors
-        gv, gl, ga = msda_backward(value, shapes, starts, loc, attn.contiguous(),
-                                   grad_out.contiguous(), accum=ctx.accum)
-        return gv, None, None, gl, ga.view_as(attn), None
+        gv, gl, ga = msda_backward(value, shapes, starts, loc, attn, grad_out.contiguous(),
+                                   accum=ctx.accum, softmax=ctx.softmax)
+        return gv, None, None, gl, ga, None, None
 
 
 def multi_scale_deformable_attention(value, spatial_shapes, level_start_index,
                                      sampling_locations, attention_weights,
-                                     accum=MSDA_ACC_FP32_BUFFER):
+                                     accum=MSDA_ACC_FP32_BUFFER, softmax=False):
     """Differentiable MSDA: value (B,S,M,D), locations (B,Q,M,L,K,2), weights
-    (B,Q,M,L,K) or (B,Q,M,L*K) -> (B,Q,M*D)."""
+    (B,Q,M,L,K) or (B,Q,M,L*K) -> (B,Q,M*D). softmax=True: the weights are
+    logits normalised over L*K inside the kernels."""
     B, Q, M, L, K, _ = sampling_locations.shape
-    attn = attention_weights.reshape(B, Q, M, L, K)
-    return MSDAFunction.apply(value, spatial_shapes, level_start_index, sampling_locations,
-                              attn, accum)
+    attn = attention_weights.reshape(B, Q, M, L, K).contiguous()
+    return MSDAFunction.apply(value.contiguous(), spatial_shapes, level_start_index,
+                              sampling_locations.contiguous(), attn, accum, softmax)
