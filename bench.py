@@ -55,6 +55,10 @@ def parse_args(argv=None):
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=50)
+    ap.add_argument("--sweep", action="store_true",
+                    help="instead of the benchmark line, time forward and backward over the "
+                         "ablation grid (B=1, bf16: Q x K x L x dispatch order, plus the "
+                         "4x4-patch contention workload), one JSON line per point")
     a = ap.parse_args(argv)
     if a.warmup < 3:
         ap.error("--warmup must be at least 3")
@@ -428,6 +432,69 @@ def run_ours(args):
     return result
 
 
+# ------------------------------------------------------------ the sweep
+
+def run_sweep(args):
+    """Median forward / backward times (L2 flushed before each timed call) over
+    the ablation grid: Q in {5000, 10000, 22223}, K in {2, 4, 8}, L in 1..4 of
+    the encoder levels, linear / Morton / Hilbert dispatch, and the
+    high-contention variant (every sample inside a 4x4-pixel patch per level)."""
+    import numpy as np
+    import torch
+
+    from scale_deformable_attention_msda_gb300 import binding, build, workloads as wl
+
+    build.build()
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    tdt = {"bf16": torch.bfloat16, "f32": torch.float32, "f16": torch.float16}[args.dtype]
+    accum = binding.MSDA_ACC_FP32_BUFFER if args.accum == "fp32_buffer" else binding.MSDA_ACC_NATIVE
+    reps = max(5, min(args.steps, 30))
+
+    def time_point(w, order_kind):
+        p = wl.make_inputs(w.with_dtype(args.dtype))
+        up = lambda a: torch.tensor(a, dtype=torch.float64).to(tdt).to(dev)  # noqa: E731
+        value, loc, attn, g = up(p["value"]), up(p["loc"]), up(p["attn"]), up(p["grad_out"])
+        shapes = torch.tensor(p["shapes"], device=dev)
+        starts = torch.tensor(p["starts"], device=dev)
+        order = None
+        if order_kind != "linear":
+            order = torch.tensor(wl.query_order(w, order_kind), device=dev)
+        out = torch.empty((w.B, w.Q, w.M * w.D), dtype=tdt, device=dev)
+        buf = binding.BackwardBuffers(value, loc, attn, accum)
+        tf, tb = [], []
+        for i in range(reps + 3):
+            flush.fill_(i & 0xff)
+            e = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+            e[0].record()
+            binding.msda_forward(value, shapes, starts, loc, attn, query_order=order, out=out)
+            e[1].record()
+            binding.msda_backward_zero(buf, tdt)
+            binding.msda_backward_accumulate(value, shapes, starts, loc, attn, g, buf,
+                                             query_order=order)
+            binding.msda_backward_finish(buf, tdt)
+            e[2].record()
+            torch.cuda.synchronize()
+            if i >= 3:
+                tf.append(e[0].elapsed_time(e[1]))
+                tb.append(e[1].elapsed_time(e[2]))
+        cb = wl.compulsory_bytes(w.with_dtype(args.dtype))
+        f, b = float(np.median(tf)), float(np.median(tb))
+        return {"workload": w.name, "Q": w.Q, "K": w.K, "L": w.L, "order": order_kind,
+                "dtype": args.dtype, "accum": args.accum, "forward_us": round(f * 1e3, 2),
+                "backward_us": round(b * 1e3, 2),
+                "queries_per_s": round(w.B * w.Q / ((f + b) * 1e-3), 1),
+                "forward_hbm_frac": round(cb["forward"] / (f * 1e-3) / 1e9 / measured_hbm_peak()[0], 4),
+                "backward_hbm_frac": round(cb["backward"] / (b * 1e-3) / 1e9 / measured_hbm_peak()[0], 4)}
+
+    for w in wl.sweep_grid():
+        for kind in ("linear", "morton", "hilbert"):
+            print(json.dumps(time_point(w, kind)), flush=True)
+    for Q in (5000, 10000, 22223):
+        print(json.dumps(time_point(wl.sweep(Q, 4, 4, contention=True), "linear")), flush=True)
+
+
 # ------------------------------------------------------- reference arm
 
 def run_reference(args):
@@ -484,7 +551,9 @@ def run_reference(args):
 
 def main(argv=None):
     args = parse_args(argv)
-    if args.impl == "reference":
+    if args.sweep:
+        run_sweep(args)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_ours(args)
