@@ -382,10 +382,14 @@ def run_ours(args):
     step_bytes = cb["forward"] + cb["backward"]
     # atomic bytes the backward adds into its accumulation target per launch
     # (every corner of every sample, at the target's element size) and the
-    # group width of one vector add: 16 bytes per lane x lanes per group
-    acc_bytes = 4 if (args.dtype == "f32" or accum == binding.MSDA_ACC_FP32_BUFFER) else 2
+    # group width of one vector add: 16 bytes per lane x lanes per group. A
+    # group has D/4 lanes for fp32 data and for 16-bit data with the fp32
+    # workspace (8-byte gathers, 4 fp32 channels added per lane, while D/4 fits
+    # a warp); D/8 lanes of 8 native 16-bit channels otherwise.
+    f32_target = args.dtype == "f32" or accum == binding.MSDA_ACC_FP32_BUFFER
+    acc_bytes = 4 if f32_target else 2
     red_bytes = w.samples * 4 * w.D * acc_bytes
-    lanes = w.D // (4 if args.dtype == "f32" else 8)
+    lanes = w.D // 4 if (f32_target and w.D // 4 <= 32) else w.D // 8
     chunk = 16 * lanes
     ceiling = RED_CEILING_GBS[128 if chunk >= 128 else 64]
     red_gbs = red_bytes / (mean["backward"] * 1e-3) / 1e9

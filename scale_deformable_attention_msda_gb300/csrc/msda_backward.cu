@@ -131,10 +131,34 @@ template <> __device__ __forceinline__ void store_xy<__half>(__half *p, float x,
 // query-heads x at most kSoftmaxSlots / GPW samples each.
 constexpr int kSoftmaxSlots = 512;
 
-template <typename T, int LPG, bool F32ACC, bool SOFTMAX>
+// A lane's share of one corner vector: 16 bytes, or 8 bytes in NARROW mode.
+template <typename T, int NB> __device__ __forceinline__ uint4 ldg_lane(const T *p) {
+    if constexpr (NB == 16) {
+        return ldg16(p);
+    } else {
+        const uint2 u = __ldg(reinterpret_cast<const uint2 *>(p));
+        return make_uint4(u.x, u.y, 0u, 0u);
+    }
+}
+template <typename T, int N> __device__ __forceinline__ void unpack_n(float *v, uint4 raw) {
+    float t[Vec16<T>::N];
+    unpack16<T>(t, raw);
+#pragma unroll
+    for (int i = 0; i < N; ++i) v[i] = t[i];
+}
+
+// NARROW (16-bit data with the fp32 workspace): 8 lanes of 8 bytes per
+// D = 32 query-head instead of 4 lanes of 16 bytes, so that each lane's
+// 16-byte fp32 add covers its 4 channels and one add instruction writes a
+// whole 128-byte workspace row per query-head (L2 reduces 128-byte groups
+// about 1.2x faster than 64-byte ones); the extra per-lane work fits in the
+// kernel's idle issue slots.
+template <typename T, int LPG, bool F32ACC, bool SOFTMAX, bool NARROW>
 __global__ void __launch_bounds__(kThreads)
 msda_backward_kernel(const Params p) {
-    constexpr int VEC = Vec16<T>::N;
+    static_assert(!NARROW || (F32ACC && sizeof(T) == 2), "narrow lanes: 16-bit data, fp32 workspace");
+    constexpr int LB = NARROW ? 8 : 16;      // bytes of one corner vector per lane
+    constexpr int VEC = LB / (int)sizeof(T);
     constexpr int GPW = 32 / LPG;
     constexpr int SPW = 64;
     constexpr int CH = SPW / GPW;
@@ -142,6 +166,7 @@ msda_backward_kernel(const Params p) {
     constexpr int U = CH < 2 ? CH : 2;
     using S = Scatter<T, F32ACC, LPG>;
     using Acc = typename S::Acc;
+    constexpr int NSC = NARROW ? VEC : S::NSC;
 
     __shared__ LevelTable lt;
     __shared__ float4 s_w[kWarpsPerBlock][SPW];
@@ -168,16 +193,21 @@ msda_backward_kernel(const Params p) {
 
     // grad_out of this query-head: the lane's gathered channels (for the dot
     // products) and the channels it scatters (zero for a group with no work)
-    float go[VEC], sc[S::NSC];
+    float go[VEC], sc[NSC];
     if (valid_q) {
         const T *grow = reinterpret_cast<const T *>(p.grad_out) + tr.bqm * p.D;
-        unpack16<T>(go, ldg16(grow + r * VEC));
-        load_scatter_g<T, F32ACC, LPG>(sc, go, grow, r);
+        unpack_n<T, VEC>(go, ldg_lane<T, LB>(grow + r * VEC));
+        if constexpr (NARROW) {
+#pragma unroll
+            for (int i = 0; i < NSC; ++i) sc[i] = go[i];
+        } else {
+            load_scatter_g<T, F32ACC, LPG>(sc, go, grow, r);
+        }
     } else {
 #pragma unroll
         for (int i = 0; i < VEC; ++i) go[i] = 0.0f;
 #pragma unroll
-        for (int i = 0; i < S::NSC; ++i) sc[i] = 0.0f;
+        for (int i = 0; i < NSC; ++i) sc[i] = 0.0f;
     }
 
     // phase-1/3 mapping as in the forward: slot lane + 32*i is sample
@@ -250,10 +280,10 @@ msda_backward_kernel(const Params p) {
             for (int u = 0; u < U; ++u) {
                 w[u] = s_w[warp][(j + u) * GPW + g];
                 o[u] = s_o[warp][(j + u) * GPW + g];
-                v[u][0] = ldg16(vbase + o[u].x);
-                v[u][1] = ldg16(vbase + o[u].y);
-                v[u][2] = ldg16(vbase + o[u].z);
-                v[u][3] = ldg16(vbase + o[u].w);
+                v[u][0] = ldg_lane<T, LB>(vbase + o[u].x);
+                v[u][1] = ldg_lane<T, LB>(vbase + o[u].y);
+                v[u][2] = ldg_lane<T, LB>(vbase + o[u].z);
+                v[u][3] = ldg_lane<T, LB>(vbase + o[u].w);
             }
 #pragma unroll
             for (int u = 0; u < U; ++u) {
@@ -261,16 +291,24 @@ msda_backward_kernel(const Params p) {
 #pragma unroll
                 for (int c = 0; c < 4; ++c) {
                     float x[VEC];
-                    unpack16<T>(x, v[u][c]);
+                    unpack_n<T, VEC>(x, v[u][c]);
                     float acc = 0.0f;
 #pragma unroll
                     for (int i = 0; i < VEC; ++i) acc = fmaf(go[i], x[i], acc);
                     d[c] = acc;
                 }
-                if (w[u].x != 0.0f) S::add(gvhead + o[u].x, w[u].x, sc, r);
-                if (w[u].y != 0.0f) S::add(gvhead + o[u].y, w[u].y, sc, r);
-                if (w[u].z != 0.0f) S::add(gvhead + o[u].z, w[u].z, sc, r);
-                if (w[u].w != 0.0f) S::add(gvhead + o[u].w, w[u].w, sc, r);
+                const float wc[4] = {w[u].x, w[u].y, w[u].z, w[u].w};
+                const int oc[4] = {o[u].x, o[u].y, o[u].z, o[u].w};
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    if (wc[c] == 0.0f) continue;
+                    if constexpr (NARROW) {
+                        float *dst = reinterpret_cast<float *>(gvhead) + oc[c] + 4 * r;
+                        red_add_v4_f32(dst, wc[c] * sc[0], wc[c] * sc[1], wc[c] * sc[2], wc[c] * sc[3]);
+                    } else {
+                        S::add(gvhead + oc[c], wc[c], sc, r);
+                    }
+                }
 #pragma unroll
                 for (int off = LPG / 2; off > 0; off >>= 1) {
 #pragma unroll
@@ -370,21 +408,40 @@ cudaError_t launch_convert(const float *ws, void *gv, int64_t n, msda_dtype_t dt
 
 template <typename T, bool F32ACC, bool SOFTMAX>
 static cudaError_t launch_backward_t(const Params &p, int lpg, cudaStream_t stream) {
-    const int gpw = 32 / lpg;
+    // 16-bit data with the fp32 workspace: twice the lanes, 8 bytes each
+    constexpr bool kNarrowable = F32ACC && sizeof(T) == 2;
+    const bool narrow = kNarrowable && 2 * lpg <= 32;
+    const int lanes = narrow ? 2 * lpg : lpg;
+    const int gpw = 32 / lanes;
     const int64_t warps = (p.triples + gpw - 1) / gpw;
     const int64_t blocks = (warps + kWarpsPerBlock - 1) / kWarpsPerBlock;
     if (blocks == 0) return cudaSuccess;
     if (blocks > 0x7fffffff) return cudaErrorInvalidConfiguration;
     const dim3 grid((unsigned)blocks);
-    switch (lpg) {
-        case 1: msda_backward_kernel<T, 1, F32ACC, SOFTMAX><<<grid, kThreads, 0, stream>>>(p); break;
-        case 2: msda_backward_kernel<T, 2, F32ACC, SOFTMAX><<<grid, kThreads, 0, stream>>>(p); break;
-        case 4: msda_backward_kernel<T, 4, F32ACC, SOFTMAX><<<grid, kThreads, 0, stream>>>(p); break;
-        case 8: msda_backward_kernel<T, 8, F32ACC, SOFTMAX><<<grid, kThreads, 0, stream>>>(p); break;
-        case 16: msda_backward_kernel<T, 16, F32ACC, SOFTMAX><<<grid, kThreads, 0, stream>>>(p); break;
-        case 32: msda_backward_kernel<T, 32, F32ACC, SOFTMAX><<<grid, kThreads, 0, stream>>>(p); break;
+#define MSDA_BWD(N, NAR) msda_backward_kernel<T, N, F32ACC, SOFTMAX, NAR><<<grid, kThreads, 0, stream>>>(p)
+    if constexpr (kNarrowable) {
+        if (narrow) {
+            switch (lanes) {
+                case 2: MSDA_BWD(2, true); break;
+                case 4: MSDA_BWD(4, true); break;
+                case 8: MSDA_BWD(8, true); break;
+                case 16: MSDA_BWD(16, true); break;
+                case 32: MSDA_BWD(32, true); break;
+                default: return cudaErrorInvalidValue;
+            }
+            return cudaGetLastError();
+        }
+    }
+    switch (lanes) {
+        case 1: MSDA_BWD(1, false); break;
+        case 2: MSDA_BWD(2, false); break;
+        case 4: MSDA_BWD(4, false); break;
+        case 8: MSDA_BWD(8, false); break;
+        case 16: MSDA_BWD(16, false); break;
+        case 32: MSDA_BWD(32, false); break;
         default: return cudaErrorInvalidValue;
     }
+#undef MSDA_BWD
     return cudaGetLastError();
 }
 

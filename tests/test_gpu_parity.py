@@ -264,6 +264,41 @@ def test_ragged_query_counts(Q):
     run_and_check(_small(Q=Q, B=3), label=f"Q={Q}")
 
 
+@pytest.mark.parametrize("dtype,D,Q,M", [("f32", 32, 1, 3), ("f32", 32, 33, 5), ("bf16", 32, 7, 3),
+                                         ("bf16", 32, 1001, 3), ("f16", 64, 5, 3),
+                                         ("f32", 128, 9, 2), ("bf16", 128, 31, 2)])
+def test_fp32_target_ragged_heads_and_orders(dtype, D, Q, M):
+    """fp32 targets with 4 channels per lane (fp32 data; 16-bit data with the
+    fp32 workspace on 8-byte lanes): ragged query counts, head counts that do
+    not divide the warp's groups, tight offsets (many shared corners), and a
+    permuted dispatch order."""
+    w = _small(Q=Q, M=M, D=D, dtype=dtype, sigma=1.0)
+    run_and_check(w, FP32BUF, label=f"D={D} Q={Q} M={M}")
+    perm = np.random.default_rng(Q).permutation(Q).astype(np.int32)
+    run_and_check(w, FP32BUF, order=perm, label=f"D={D} Q={Q} M={M} permuted")
+
+
+@pytest.mark.parametrize("w", [wl.sweep(5000, 4, 4), wl.sweep(5000, 4, 4, contention=True),
+                               wl.sweep(5000, 4, 4, dtype="f32")],
+                         ids=lambda w: f"{w.name}-{w.dtype}")
+def test_grad_value_elementwise_bound(w):
+    """Every grad_value element within a bound of the sum of the magnitudes
+    of its contributions, sum |a w_c g| (the oracle backward with |grad_out|):
+    a dropped, duplicated or misrouted contribution breaks it in any row with
+    few contributions, where a tensor-wide relative norm could miss it."""
+    p = wl.make_inputs(w)
+    got = gpu_run(p, w.dtype, FP32BUF)
+    ref = oracle_run(p)
+    mag, _, _ = oracle.backward(p["value"], p["shapes"], p["starts"], p["loc"], p["attn"],
+                                np.abs(p["grad_out"]))
+    # fp32 sums of at most a few thousand terms, then (16-bit) one rounding
+    rel = 1e-4 if w.dtype == "f32" else 2.0 ** -8 + 1e-4
+    err = np.abs(got["gv"] - ref["gv"])
+    bound = rel * mag + 1e-30
+    worst = float(np.max(err / bound))
+    assert worst <= 1.0, (w.name, w.dtype, worst)
+
+
 @pytest.mark.parametrize("K,levels", [(1, ((5, 6),)), (1, ((1, 1),)), (16, ((3, 2), (1, 4))),
                                       (5, tuple((2 + l, 3 + l) for l in range(16)))])
 def test_level_and_point_counts(K, levels):
