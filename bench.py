@@ -210,6 +210,38 @@ def profiled_traffic(kernel: str):
     return int(m.group(1)) if m.group(2) == kernel_source_hash(kernel) else None
 
 
+def issued_atomic_bytes(p, D: int, acc_bytes: int, block: int) -> int:
+    """Bytes the backward's vector adds carry into its accumulation target in
+    one launch: D channels of acc_bytes for every distinct in-map corner row
+    among the corners of each aligned block of `block` consecutive samples of
+    one query-head (the kernel sums the weights of corners that share a row
+    there and adds once). Counted here with numpy from the inputs, for the
+    atomic roofline only."""
+    import numpy as np
+    loc = np.asarray(p["loc"], dtype=np.float64)                 # (B, Q, M, L, K, 2)
+    H = np.asarray(p["shapes"])[:, 0][None, None, None, :, None]
+    W = np.asarray(p["shapes"])[:, 1][None, None, None, :, None]
+    start = np.asarray(p["starts"])[None, None, None, :, None]
+    x0 = np.floor(loc[..., 0] * W - 0.5).astype(np.int64)
+    y0 = np.floor(loc[..., 1] * H - 0.5).astype(np.int64)
+    rows = []
+    for dy in (0, 1):
+        for dx in (0, 1):
+            xx, yy = x0 + dx, y0 + dy
+            ok = (xx >= 0) & (xx < W) & (yy >= 0) & (yy < H)
+            rows.append(np.where(ok, start + yy * W + xx, -1))
+    B, Q, M, L, K = x0.shape
+    r = np.stack(rows, -1).reshape(B * Q * M, L * K, 4)
+    n_blocks = (L * K + block - 1) // block
+    pad = n_blocks * block - L * K
+    if pad:
+        r = np.concatenate([r, np.full((B * Q * M, pad, 4), -1, np.int64)], axis=1)
+    r = np.sort(r.reshape(B * Q * M, n_blocks, block * 4), axis=-1)
+    first = np.ones(r.shape, dtype=bool)
+    first[..., 1:] = r[..., 1:] != r[..., :-1]
+    return int(np.count_nonzero(first & (r >= 0))) * D * acc_bytes
+
+
 # ---------------------------------------------------------- CPU baseline
 
 def cpu_baseline(p, seconds: float = 10.0, max_reps: int = 20, nthreads: int = 0):
@@ -430,14 +462,15 @@ def run_ours(args):
     # a warp); D/8 lanes of 8 native 16-bit channels otherwise.
     f32_target = args.dtype == "f32" or accum == binding.MSDA_ACC_FP32_BUFFER
     acc_bytes = 4 if f32_target else 2
-    red_bytes = w.samples * 4 * w.D * acc_bytes
     lanes = w.D // 4 if (f32_target and w.D // 4 <= 32) else w.D // 8
     chunk = 16 * lanes
+    red_bytes = issued_atomic_bytes(p, w.D, acc_bytes, min(4, lanes))
     ceiling = RED_CEILING_GBS[128 if chunk >= 128 else 64]
     red_gbs = red_bytes / (mean["backward"] * 1e-3) / 1e9
     atomic_roofline = {"kernel": "msda_backward_kernel", "bound": "l2_reduction",
                        "achieved": round(red_gbs, 1), "peak": ceiling, "unit": "GB/s",
                        "frac": round(red_gbs / ceiling, 4), "atomic_bytes": red_bytes,
+                       "atomic_bytes_unmerged": w.samples * 4 * w.D * acc_bytes,
                        "peak_source": "measured red.global.add.v4 throughput, "
                                       f"{chunk}-byte groups (probes/memprobe.cu)"}
 
