@@ -59,6 +59,11 @@ def parse_args(argv=None):
                     help="instead of the benchmark line, time forward and backward over the "
                          "ablation grid (B=1, bf16: Q x K x L x dispatch order, plus the "
                          "4x4-patch contention workload), one JSON line per point")
+    ap.add_argument("--configs", action="store_true",
+                    help="instead of the benchmark line, time forward and backward (cold "
+                         "and warm L2) on the decoder, encoder and Mask2Former "
+                         "configurations, with the fp64 oracle on 1 thread and all cores, "
+                         "one JSON line per configuration")
     a = ap.parse_args(argv)
     if a.warmup < 3:
         ap.error("--warmup must be at least 3")
@@ -574,6 +579,99 @@ def run_sweep(args):
         print(json.dumps(time_point(wl.sweep(Q, 4, 4, contention=True), "linear")), flush=True)
 
 
+def run_configs(args):
+    """Per configuration: median forward and backward call times (msda_forward,
+    msda_backward = zero + accumulate + finish) over 50 calls after 10
+    warm-up, cold (L2 flushed before each call) and warm (not flushed); their
+    HBM fractions; and the fp64 oracle on the host, one thread and all cores."""
+    import numpy as np
+    import torch
+
+    import oracle
+    from scale_deformable_attention_msda_gb300 import binding, build, workloads as wl
+
+    build.build()
+    oracle.build()
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    peak = measured_hbm_peak()[0]
+    plan = [(wl.decoder, "f32", "fp32_buffer"), (wl.decoder, "bf16", "fp32_buffer"),
+            (wl.encoder, "f32", "fp32_buffer"), (wl.encoder, "bf16", "fp32_buffer"),
+            (wl.encoder, "bf16", "native"), (wl.mask2former, "bf16", "fp32_buffer"),
+            (wl.mask2former, "bf16", "native")]
+    for make, dtype, acc_name in plan:
+        w = make(dtype)
+        p = wl.make_inputs(w)
+        tdt = {"bf16": torch.bfloat16, "f32": torch.float32, "f16": torch.float16}[dtype]
+        accum = (binding.MSDA_ACC_FP32_BUFFER if acc_name == "fp32_buffer"
+                 else binding.MSDA_ACC_NATIVE)
+        up = lambda a: torch.tensor(a, dtype=torch.float64).to(tdt).to(dev)  # noqa: E731
+        value, loc, attn, g = up(p["value"]), up(p["loc"]), up(p["attn"]), up(p["grad_out"])
+        shapes = torch.tensor(p["shapes"], device=dev)
+        starts = torch.tensor(p["starts"], device=dev)
+        out = torch.empty((w.B, w.Q, w.M * w.D), dtype=tdt, device=dev)
+        buf = binding.BackwardBuffers(value, loc, attn, accum)
+
+        def fwd():
+            binding.msda_forward(value, shapes, starts, loc, attn, out=out)
+
+        def bwd():
+            binding.msda_backward(value, shapes, starts, loc, attn, g, accum=accum,
+                                  grad_value=buf.grad_value,
+                                  grad_sampling_locations=buf.grad_sampling_locations,
+                                  grad_attention_weights=buf.grad_attention_weights,
+                                  workspace=buf.workspace)
+
+        def median_us(fn, cold):
+            ts = []
+            for i in range(60):
+                if cold:
+                    flush.fill_(i & 0xff)
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record()
+                fn()
+                b.record()
+                torch.cuda.synchronize()
+                if i >= 10:
+                    ts.append(a.elapsed_time(b) * 1e3)
+            return float(np.median(ts))
+
+        t = {f"{n}_{c}_us": round(median_us(fn, c == "cold"), 2)
+             for n, fn in (("forward", fwd), ("backward", bwd)) for c in ("cold", "warm")}
+        cb = wl.compulsory_bytes(w)
+        f64 = {k: np.ascontiguousarray(p[k], dtype=np.float64)
+               for k in ("value", "loc", "attn", "grad_out")}
+
+        def oracle_s(nthreads):
+            r = {}
+            for name, fn in (("forward", lambda: oracle.forward(
+                                 f64["value"], p["shapes"], p["starts"], f64["loc"], f64["attn"],
+                                 nthreads=nthreads)),
+                             ("backward", lambda: oracle.backward(
+                                 f64["value"], p["shapes"], p["starts"], f64["loc"], f64["attn"],
+                                 f64["grad_out"], nthreads=nthreads))):
+                ts = []
+                while len(ts) < 3 and sum(ts) < 20.0:
+                    t0 = time.perf_counter()
+                    fn()
+                    ts.append(time.perf_counter() - t0)
+                r[name] = float(np.median(ts))
+            return r
+
+        one, allc = oracle_s(1), oracle_s(0)
+        q = w.B * w.Q
+        print(json.dumps({
+            "config": w.name, "dtype": dtype, "accum": acc_name if dtype != "f32" else "fp32",
+            "B": w.B, "Q": w.Q, "S": w.S, "samples": w.samples, **t,
+            "queries_per_s_cold": round(q / ((t["forward_cold_us"] + t["backward_cold_us"]) * 1e-6), 1),
+            "forward_hbm_frac_cold": round(cb["forward"] / (t["forward_cold_us"] * 1e-6) / 1e9 / peak, 4),
+            "backward_hbm_frac_cold": round(cb["backward"] / (t["backward_cold_us"] * 1e-6) / 1e9 / peak, 4),
+            "oracle_1_thread_queries_per_s": round(q / (one["forward"] + one["backward"]), 1),
+            "oracle_all_cores_queries_per_s": round(q / (allc["forward"] + allc["backward"]), 1),
+            "oracle_cores": os.cpu_count() or 1}), flush=True)
+
+
 # ------------------------------------------------------- reference arm
 
 def run_reference(args):
@@ -632,6 +730,8 @@ def main(argv=None):
     args = parse_args(argv)
     if args.sweep:
         run_sweep(args)
+    elif args.configs:
+        run_configs(args)
     elif args.impl == "reference":
         run_reference(args)
     else:
