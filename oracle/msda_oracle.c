@@ -49,9 +49,11 @@ static int dims_ok(int64_t B, int64_t S, int64_t Q, int64_t M, int64_t D,
            L <= ORACLE_MAX_LEVELS && K >= 1;
 }
 
+/* nthreads > 0: that many OpenMP threads; 0: every processor (set each call,
+ * since the OpenMP thread count persists between calls). */
 static void set_threads(int nthreads) {
 #ifdef _OPENMP
-    if (nthreads > 0) omp_set_num_threads(nthreads);
+    omp_set_num_threads(nthreads > 0 ? nthreads : omp_get_num_procs());
 #else
     (void)nthreads;
 #endif
