@@ -181,6 +181,9 @@ def measured_hbm_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
+ACCUM_MODES = {"fp32_buffer": lambda b: b.MSDA_ACC_FP32_BUFFER,
+               "native": lambda b: b.MSDA_ACC_NATIVE}
+
 KERNEL_SOURCES = {"msda_forward_kernel": ("msda_common.cuh", "msda_forward.cu"),
                   "msda_backward_kernel": ("msda_common.cuh", "msda_backward.cu")}
 
@@ -215,13 +218,14 @@ def profiled_traffic(kernel: str):
     return int(m.group(1)) if m.group(2) == kernel_source_hash(kernel) else None
 
 
-def issued_atomic_bytes(p, D: int, acc_bytes: int, block: int) -> int:
-    """Bytes the backward's vector adds carry into its accumulation target in
-    one launch: D channels of acc_bytes for every distinct in-map corner row
-    among the corners of each aligned block of `block` consecutive samples of
-    one query-head (the kernel sums the weights of corners that share a row
-    there and adds once). Counted here with numpy from the inputs, for the
-    atomic roofline only."""
+def issued_atomic_rows(p, block: int):
+    """Per level, the vector adds the backward issues per launch: every
+    distinct in-map corner row among the corners of each aligned block of
+    `block` consecutive samples of one query-head (the kernel sums the
+    weights of corners that share a row there and adds once), counted with
+    numpy from the inputs, for the atomic roofline only. A block is counted
+    under the level of its first sample (one level exactly when K is a
+    multiple of `block`)."""
     import numpy as np
     loc = np.asarray(p["loc"], dtype=np.float64)                 # (B, Q, M, L, K, 2)
     H = np.asarray(p["shapes"])[:, 0][None, None, None, :, None]
@@ -244,7 +248,9 @@ def issued_atomic_bytes(p, D: int, acc_bytes: int, block: int) -> int:
     r = np.sort(r.reshape(B * Q * M, n_blocks, block * 4), axis=-1)
     first = np.ones(r.shape, dtype=bool)
     first[..., 1:] = r[..., 1:] != r[..., :-1]
-    return int(np.count_nonzero(first & (r >= 0))) * D * acc_bytes
+    per_block = np.count_nonzero(first & (r >= 0), axis=(0, 2))   # (n_blocks,)
+    level_of_block = (np.arange(n_blocks) * block) // K
+    return [int(per_block[level_of_block == l].sum()) for l in range(L)]
 
 
 # ---------------------------------------------------------- CPU baseline
@@ -363,7 +369,7 @@ def run_ours(args):
     binding.lib()
 
     tdt = {"bf16": torch.bfloat16, "f32": torch.float32, "f16": torch.float16}[args.dtype]
-    accum = binding.MSDA_ACC_FP32_BUFFER if args.accum == "fp32_buffer" else binding.MSDA_ACC_NATIVE
+    accum = ACCUM_MODES[args.accum](binding)
     w = wl.encoder(args.dtype, variant=rank)
     p = wl.make_inputs(w)
 
@@ -459,31 +465,35 @@ def run_ours(args):
             k.update(algorithmic_bytes=algo[n], gbs=round(gbs, 1), hbm_frac=round(gbs / peak, 4))
         kernels[n] = k
     step_bytes = cb["forward"] + cb["backward"]
-    # atomic bytes the backward adds into its accumulation target per launch
-    # (every corner of every sample, at the target's element size) and the
-    # group width of one vector add: 16 bytes per lane x lanes per group. A
-    # group has D/4 lanes for fp32 data and for 16-bit data with the fp32
-    # workspace (8-byte gathers, 4 fp32 channels added per lane, while D/4 fits
-    # a warp); D/8 lanes of 8 native 16-bit channels otherwise.
+    # Atomic bytes the backward adds per launch (the distinct corner rows it
+    # issues, at the target's element size) and the bytes one add instruction
+    # covers per query-head. fp32 data and 16-bit data with the fp32
+    # workspace use D/4 lanes of 4 fp32 channels while D/4 fits a warp (4 D
+    # bytes per query-head; 16-byte lanes with 16-bit data write 2 D, in two
+    # halves); native 16-bit mode uses D/8 lanes of 8 channels (2 D bytes).
     f32_target = args.dtype == "f32" or accum == binding.MSDA_ACC_FP32_BUFFER
+    narrow = f32_target and w.D // 4 <= 32
+    lanes = w.D // 4 if narrow else w.D // 8
     acc_bytes = 4 if f32_target else 2
-    lanes = w.D // 4 if (f32_target and w.D // 4 <= 32) else w.D // 8
-    chunk = 16 * lanes
-    red_bytes = issued_atomic_bytes(p, w.D, acc_bytes, min(4, lanes))
-    ceiling = RED_CEILING_GBS[128 if chunk >= 128 else 64]
+    rows_per_level = issued_atomic_rows(p, min(4, lanes))
+    red_bytes = sum(rows_per_level) * w.D * acc_bytes
+    group = (4 if narrow else 2) * w.D
+    ceiling = RED_CEILING_GBS[128 if group >= 128 else 64]
     red_gbs = red_bytes / (mean["backward"] * 1e-3) / 1e9
     atomic_roofline = {"kernel": "msda_backward_kernel", "bound": "l2_reduction",
                        "achieved": round(red_gbs, 1), "peak": ceiling, "unit": "GB/s",
                        "frac": round(red_gbs / ceiling, 4), "atomic_bytes": red_bytes,
                        "atomic_bytes_unmerged": w.samples * 4 * w.D * acc_bytes,
+                       "atomic_bytes_per_level": [n * w.D * acc_bytes for n in rows_per_level],
                        "peak_source": "measured red.global.add.v4 throughput, "
-                                      f"{chunk}-byte groups (probes/memprobe.cu)"}
+                                      f"{group}-byte groups (probes/memprobe.cu)"}
 
     result = None
     if rank == 0:
         cpu = None
         if world == 1 and not args.no_cpu_baseline:
             cpu = cpu_baseline(p)
+        # forward, zero (grad_value and/or workspace), accumulate, finish
         launches_per_step = 4 if (args.dtype != "f32" and accum == binding.MSDA_ACC_FP32_BUFFER) else 3
         result = {
             "metric": METRIC, "value": round(qps, 1), "unit": UNIT, "n_gpus": world,
@@ -533,7 +543,7 @@ def run_sweep(args):
     torch.cuda.set_device(dev)
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
     tdt = {"bf16": torch.bfloat16, "f32": torch.float32, "f16": torch.float16}[args.dtype]
-    accum = binding.MSDA_ACC_FP32_BUFFER if args.accum == "fp32_buffer" else binding.MSDA_ACC_NATIVE
+    accum = ACCUM_MODES[args.accum](binding)
     reps = max(5, min(args.steps, 30))
 
     def time_point(w, order_kind):
@@ -604,8 +614,7 @@ def run_configs(args):
         w = make(dtype)
         p = wl.make_inputs(w)
         tdt = {"bf16": torch.bfloat16, "f32": torch.float32, "f16": torch.float16}[dtype]
-        accum = (binding.MSDA_ACC_FP32_BUFFER if acc_name == "fp32_buffer"
-                 else binding.MSDA_ACC_NATIVE)
+        accum = ACCUM_MODES[acc_name](binding)
         up = lambda a: torch.tensor(a, dtype=torch.float64).to(tdt).to(dev)  # noqa: E731
         value, loc, attn, g = up(p["value"]), up(p["loc"]), up(p["attn"]), up(p["grad_out"])
         shapes = torch.tensor(p["shapes"], device=dev)
