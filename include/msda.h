@@ -91,7 +91,8 @@ typedef enum {
     MSDA_ERR_DTYPE = 3,     /* unknown dtype or accumulation mode              */
     MSDA_ERR_ALIGN = 4,     /* a pointer is not aligned as required            */
     MSDA_ERR_WORKSPACE = 5, /* workspace missing or smaller than required      */
-    MSDA_ERR_CUDA = 6       /* the CUDA runtime rejected a launch              */
+    MSDA_ERR_CUDA = 6,      /* the CUDA runtime rejected a launch              */
+    MSDA_ERR_DEVICE_BOUNDS = 7  /* checked build: a kernel access left its tensor */
 } msda_status_t;
 
 /* Problem sizes. Supported: B >= 0, Q >= 0 (zero is a valid empty call),
@@ -252,6 +253,27 @@ MSDA_API msda_status_t msda_debug_corners(const int64_t *spatial_shapes,
                                  const void *sampling_locations,
                                  int32_t *corner_rows, const msda_dims_t *dims,
                                  msda_dtype_t dtype, void *stream);
+
+/* Range-checked build. libmsda_checked.so is built from the same sources
+ * with every global access of every kernel first checked against the extent
+ * of its tensor (derived from dims): an access that would leave its tensor is
+ * skipped -- a load yields zeros, a store or add does nothing -- and a
+ * per-device fault word is set; nothing traps. It is a debugging stand-in for
+ * a memory checker, much slower than libmsda.so. The normal library exports
+ * the same three entry points and never sets the word.
+ * msda_checked_build: 1 in libmsda_checked.so, 0 in libmsda.so.
+ * msda_device_check: synchronizes `stream`, then reads and clears the current
+ *   device's fault word: MSDA_ERR_DEVICE_BOUNDS if any checked access was
+ *   out of range since the last call, MSDA_OK otherwise (always in the normal
+ *   build); MSDA_ERR_CUDA if the synchronization or the readback fails.
+ * msda_debug_bounds_self_test: enqueues one range check that must fail (no
+ *   memory is accessed), so that the next msda_device_check of the checked
+ *   build returns MSDA_ERR_DEVICE_BOUNDS; a no-op check in the normal build.
+ * The first call on each device looks up the word's device address; make it
+ * before any stream capture begins. */
+MSDA_API int msda_checked_build(void);
+MSDA_API msda_status_t msda_device_check(void *stream);
+MSDA_API msda_status_t msda_debug_bounds_self_test(void *stream);
 
 /* Static description of a status code (never NULL). */
 MSDA_API const char *msda_status_string(msda_status_t status);

@@ -21,11 +21,14 @@ MSDA_ACC_NATIVE, MSDA_ACC_FP32_BUFFER = 0, 1
 _DTYPES = {torch.float32: MSDA_F32, torch.bfloat16: MSDA_BF16, torch.float16: MSDA_F16,
            torch.float64: MSDA_F64}
 STATUS = {0: "MSDA_OK", 1: "MSDA_ERR_NULL", 2: "MSDA_ERR_SHAPE", 3: "MSDA_ERR_DTYPE",
-          4: "MSDA_ERR_ALIGN", 5: "MSDA_ERR_WORKSPACE", 6: "MSDA_ERR_CUDA"}
+          4: "MSDA_ERR_ALIGN", 5: "MSDA_ERR_WORKSPACE", 6: "MSDA_ERR_CUDA",
+          7: "MSDA_ERR_DEVICE_BOUNDS"}
+MSDA_ERR_DEVICE_BOUNDS = 7
 EXPORTED = ("msda_forward", "msda_backward_workspace_bytes", "msda_backward",
             "msda_backward_zero", "msda_backward_accumulate", "msda_backward_finish",
             "msda_backward_static_workspace", "msda_forward_softmax", "msda_backward_softmax",
-            "msda_debug_corners", "msda_status_string", "msda_version")
+            "msda_debug_corners", "msda_checked_build", "msda_device_check",
+            "msda_debug_bounds_self_test", "msda_status_string", "msda_version")
 
 
 class msda_dims_t(ctypes.Structure):
@@ -79,11 +82,27 @@ def load(path: str | None = None):
     so.msda_backward_static_workspace.restype = ctypes.c_int
     so.msda_debug_corners.argtypes = [vp, vp, vp, vp, dims, ctypes.c_int, vp]
     so.msda_debug_corners.restype = ctypes.c_int
+    so.msda_checked_build.argtypes = []
+    so.msda_checked_build.restype = ctypes.c_int
+    so.msda_device_check.argtypes = [vp]
+    so.msda_device_check.restype = ctypes.c_int
+    so.msda_debug_bounds_self_test.argtypes = [vp]
+    so.msda_debug_bounds_self_test.restype = ctypes.c_int
     so.msda_status_string.argtypes = [ctypes.c_int]
     so.msda_status_string.restype = ctypes.c_char_p
     so.msda_version.argtypes = []
     so.msda_version.restype = ctypes.c_int
     return so
+
+
+def use_library(path: str | None = None):
+    """Make every call of this module go to the library at `path` (default:
+    libmsda.so), e.g. the range-checked build at build.CHECKED_LIBRARY;
+    returns its handle."""
+    global _lib
+    with _lock:
+        _lib = load(path)
+    return _lib
 
 
 def lib():
@@ -230,6 +249,22 @@ def msda_backward_finish(buf: BackwardBuffers, dtype, stream=None):
     _call("msda_backward_finish", lib().msda_backward_finish(
         _ptr(buf.workspace), ctypes.c_size_t(buf.workspace_bytes), _ptr(buf.grad_value),
         buf.accum, ctypes.byref(buf.dims), _DTYPES[dtype], _stream(stream)))
+
+
+def msda_device_check(stream=None) -> int:
+    """Synchronize `stream`, then read and clear the range-fault word of the
+    checked build: returns MSDA_OK (0) or MSDA_ERR_DEVICE_BOUNDS (7); always
+    0 with the normal library. Raises on a CUDA failure."""
+    st = int(lib().msda_device_check(_stream(stream)))
+    if st not in (0, MSDA_ERR_DEVICE_BOUNDS):
+        raise MSDAError(st, "msda_device_check")
+    return st
+
+
+def msda_debug_bounds_self_test(stream=None):
+    """Enqueue one range check that must fail (no memory access): the next
+    msda_device_check of the checked build returns MSDA_ERR_DEVICE_BOUNDS."""
+    _call("msda_debug_bounds_self_test", lib().msda_debug_bounds_self_test(_stream(stream)))
 
 
 def msda_debug_corners(spatial_shapes, level_start_index, sampling_locations, S: int,

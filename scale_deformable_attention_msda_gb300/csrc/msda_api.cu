@@ -16,6 +16,7 @@ cudaError_t launch_corners(const Params &p, msda_dtype_t dt, int32_t *rows, cuda
 cudaError_t launch_forward_f64(const Params &p, int lpg, bool softmax, cudaStream_t stream);
 cudaError_t launch_backward_f64(const Params &p, int lpg, bool softmax, cudaStream_t stream);
 cudaError_t launch_corners_f64(const Params &p, int32_t *rows, cudaStream_t stream);
+cudaError_t fault_word_for_launch(unsigned **err);
 }  // namespace msda
 
 namespace {
@@ -115,6 +116,8 @@ const char *msda_status_string(msda_status_t s) {
         case MSDA_ERR_ALIGN: return "a pointer is not aligned as required";
         case MSDA_ERR_WORKSPACE: return "workspace missing or too small";
         case MSDA_ERR_CUDA: return "the CUDA runtime rejected a launch";
+        case MSDA_ERR_DEVICE_BOUNDS:
+            return "checked build: a kernel access fell outside its tensor";
     }
     return "unknown status";
 }
@@ -136,6 +139,7 @@ static msda_status_t forward_impl(const void *value, const int64_t *spatial_shap
     if (!out) return MSDA_ERR_NULL;
     if (!aligned(out, 16) || (query_order && !aligned(query_order, 4))) return MSDA_ERR_ALIGN;
     Params p = make_params(d);
+    if (msda::fault_word_for_launch(&p.err) != cudaSuccess) return MSDA_ERR_CUDA;
     p.value = value;
     p.shapes = spatial_shapes;
     p.starts = level_start_index;
@@ -244,6 +248,7 @@ static msda_status_t accumulate_impl(const void *value, const int64_t *spatial_s
         (query_order && !aligned(query_order, 4)))
         return MSDA_ERR_ALIGN;
     Params p = make_params(d);
+    if (msda::fault_word_for_launch(&p.err) != cudaSuccess) return MSDA_ERR_CUDA;
     p.value = value;
     p.shapes = spatial_shapes;
     p.starts = level_start_index;
@@ -384,6 +389,7 @@ msda_status_t msda_debug_corners(const int64_t *spatial_shapes, const int64_t *l
     p.LK = (int)(d.L * d.K);
     p.inv_K = 1.0f / (float)d.K;
     p.triples = d.B * d.Q * d.M;
+    if (msda::fault_word_for_launch(&p.err) != cudaSuccess) return MSDA_ERR_CUDA;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     return from_cuda(dtype == MSDA_F64 ? msda::launch_corners_f64(p, corner_rows, s)
                                        : msda::launch_corners(p, dtype, corner_rows, s));

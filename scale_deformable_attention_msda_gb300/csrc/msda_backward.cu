@@ -231,14 +231,18 @@ msda_backward_kernel(const Params p) {
     const Triple tr = triple_of(active ? t : t0, p);
     const bool valid_q = active && tr.q >= 0 && tr.q < p.Q;
     const int64_t head = ((int64_t)tr.b * p.S * p.M + tr.m) * p.D;    // row 0 of this head
-    const T *vbase = reinterpret_cast<const T *>(p.value) + head + r * VEC;
-    Acc *gvhead = reinterpret_cast<Acc *>(p.grad_value) + head;
+    const T *value = reinterpret_cast<const T *>(p.value);
+    const T *vbase = value + head + r * VEC;
+    Acc *gvbase = reinterpret_cast<Acc *>(p.grad_value);
+    Acc *gvhead = gvbase + head;
+    const int64_t nv = n_value(p), ns = n_samples(p);
 
     // grad_out of this query-head: the lane's gathered channels (for the dot
     // products) and the channels it scatters (zero for a group with no work)
     float go[VEC], sc[NSC];
-    if (valid_q) {
-        const T *grow = reinterpret_cast<const T *>(p.grad_out) + tr.bqm * p.D;
+    const T *gout = reinterpret_cast<const T *>(p.grad_out);
+    if (valid_q && in_tensor(p, gout, gout + tr.bqm * p.D, p.D, n_out(p))) {
+        const T *grow = gout + tr.bqm * p.D;
         unpack_n<T, VEC>(go, ldg_lane<T, LB>(grow + r * VEC));
         if constexpr (NARROW) {
 #pragma unroll
@@ -269,7 +273,8 @@ msda_backward_kernel(const Params p) {
     // With SOFTMAX, attn holds logits and grad_attn receives d loss / d logit:
     // a = softmax(logits), g_logit = a * (g_a - sum_j a_j g_a_j).
     SoftmaxStats sm = {0.0f, 1.0f};
-    if (SOFTMAX) sm = softmax_stats<T, LPG>(attn + trp.bqm * p.LK, prep_ok ? p.LK : 0, lane);
+    const bool logits_ok = prep_ok && in_tensor(p, attn, attn + trp.bqm * p.LK, p.LK, ns);
+    if (SOFTMAX) sm = softmax_stats<T, LPG>(attn + trp.bqm * p.LK, logits_ok ? p.LK : 0, lane);
     float sum_ag = 0.0f;
 
     for (int base = 0; base < p.LK; base += CH) {
@@ -285,9 +290,11 @@ msda_backward_kernel(const Params p) {
             f_mask[i] = 0u;
             if (prep_ok && idx < p.LK) {
                 const int64_t e = trp.bqm * p.LK + idx;
-                const float2 xy = load_xy<T>(loc + 2 * e);
-                const float a = SOFTMAX ? softmax_weight(load_scalar<T>(attn + e), sm)
-                                        : load_scalar<T>(attn + e);
+                const float2 xy = in_tensor(p, loc, loc + 2 * e, 2, 2 * ns)
+                                      ? load_xy<T>(loc + 2 * e) : make_float2(0.f, 0.f);
+                const float z = in_tensor(p, attn, attn + e, 1, ns) ? load_scalar<T>(attn + e)
+                                                                     : 0.0f;
+                const float a = SOFTMAX ? softmax_weight(z, sm) : z;
                 const int l = level_of(idx, p.inv_K);
                 SampleGeom sg;
                 sample_geometry(sg, xy.x, xy.y, lt, l);
@@ -324,10 +331,15 @@ msda_backward_kernel(const Params p) {
             for (int u = 0; u < U; ++u) {
                 w[u] = s_w[warp][(j + u) * GPW + g];
                 o[u] = s_o[warp][(j + u) * GPW + g];
-                v[u][0] = ldg_lane<T, LB>(vbase + o[u].x);
-                v[u][1] = ldg_lane<T, LB>(vbase + o[u].y);
-                v[u][2] = ldg_lane<T, LB>(vbase + o[u].z);
-                v[u][3] = ldg_lane<T, LB>(vbase + o[u].w);
+                const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
+                v[u][0] = in_tensor(p, value, vbase + o[u].x, VEC, nv)
+                              ? ldg_lane<T, LB>(vbase + o[u].x) : zero;
+                v[u][1] = in_tensor(p, value, vbase + o[u].y, VEC, nv)
+                              ? ldg_lane<T, LB>(vbase + o[u].y) : zero;
+                v[u][2] = in_tensor(p, value, vbase + o[u].z, VEC, nv)
+                              ? ldg_lane<T, LB>(vbase + o[u].z) : zero;
+                v[u][3] = in_tensor(p, value, vbase + o[u].w, VEC, nv)
+                              ? ldg_lane<T, LB>(vbase + o[u].w) : zero;
             }
 #pragma unroll
             for (int u = 0; u < U; ++u) {
@@ -345,7 +357,8 @@ msda_backward_kernel(const Params p) {
                 const int oc[4] = {o[u].x, o[u].y, o[u].z, o[u].w};
 #pragma unroll
                 for (int c = 0; c < 4; ++c) {
-                    if (wc[c] == 0.0f) continue;
+                    // the group adds within the D channels of one head's row
+                    if (wc[c] == 0.0f || !in_tensor(p, gvbase, gvhead + oc[c], p.D, nv)) continue;
                     if constexpr (NARROW) {
                         float *dst = reinterpret_cast<float *>(gvhead) + oc[c] + 4 * r;
                         red_add_v4_f32(dst, wc[c] * sc[0], wc[c] * sc[1], wc[c] * sc[2], wc[c] * sc[3]);
@@ -378,12 +391,15 @@ msda_backward_kernel(const Params p) {
                 const float dly = hx * (s10 - s00) + lx * (s11 - s01);
                 const int64_t e = trp.bqm * p.LK + idx;
                 if (SOFTMAX) {
-                    s_ga[warp][pg * SLOTS + idx] = ga;
+                    float *slot = &s_ga[warp][pg * SLOTS + idx];
+                    if (in_tensor(p, &s_ga[warp][0], slot, 1, SOFTMAX ? kSoftmaxSlots : 1))
+                        *slot = ga;
                     sum_ag += f_a[i] * ga;
-                } else {
+                } else if (in_tensor(p, gattn, gattn + e, 1, ns)) {
                     gattn[e] = Elem<T>::from_f(ga);
                 }
-                store_xy<T>(gloc + 2 * e, f_a[i] * f_W[i] * dlx, f_a[i] * f_H[i] * dly);
+                if (in_tensor(p, gloc, gloc + 2 * e, 2, 2 * ns))
+                    store_xy<T>(gloc + 2 * e, f_a[i] * f_W[i] * dlx, f_a[i] * f_H[i] * dly);
             }
         }
         __syncwarp();
@@ -397,6 +413,10 @@ msda_backward_kernel(const Params p) {
         if (prep_ok) {
             for (int idx = pj; idx < p.LK; idx += LPG) {
                 const int64_t e = trp.bqm * p.LK + idx;
+                if (!in_tensor(p, gattn, gattn + e, 1, ns) || !in_tensor(p, attn, attn + e, 1, ns) ||
+                    !in_tensor(p, &s_ga[warp][0], &s_ga[warp][pg * SLOTS + idx], 1,
+                               SOFTMAX ? kSoftmaxSlots : 1))
+                    continue;
                 const float a = softmax_weight(load_scalar<T>(attn + e), sm);
                 gattn[e] = Elem<T>::from_f(a * (s_ga[warp][pg * SLOTS + idx] - sum_ag));
             }

@@ -1,0 +1,103 @@
+// The range-checked build's fault word and its readback (libmsda_checked.so,
+// compiled with -DMSDA_CHECKED; the normal libmsda.so has the same entry
+// points, which then report no faults).
+//
+// compute-sanitizer is not available where this library is tested, so the
+// checked build stands in for its memcheck: every global access of every
+// kernel is checked first against the extent of the tensor it belongs to
+// (in_tensor in msda_common.cuh). An access that would leave its tensor is
+// skipped and sets bit 0 of one device word per GPU; the host reads and
+// clears that word after a synchronisation. Nothing traps, so a fault found
+// this way leaves the context usable.
+//
+// The word is a file-scope __device__ variable. Host code cannot use its name
+// as a device address, so the first call on each device looks the address up
+// with cudaGetSymbolAddress (that device current) and caches it; make that
+// first call before any stream capture begins.
+#include <mutex>
+
+#include "msda_common.cuh"
+
+namespace msda {
+
+namespace {
+
+__device__ unsigned g_fault_word;
+
+constexpr int kMaxDevices = 64;
+std::mutex g_lock;
+unsigned *g_address[kMaxDevices] = {};
+
+cudaError_t fault_word_address(unsigned **out) {
+    int dev = -1;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> guard(g_lock);
+    if (!g_address[dev]) {
+        void *p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_fault_word);
+        if (e != cudaSuccess) return e;
+        g_address[dev] = static_cast<unsigned *>(p);
+    }
+    *out = g_address[dev];
+    return cudaSuccess;
+}
+
+// One range check that must fail (a NULL tensor of extent 0); no memory access.
+__global__ void bounds_self_test_kernel(const Params p) {
+    if (threadIdx.x == 0) (void)in_tensor(p, static_cast<const int *>(nullptr),
+                                          static_cast<const int *>(nullptr), 1, 0);
+}
+
+}  // namespace
+
+// Params::err for a launch: the current device's fault word in the checked
+// build, NULL in the normal one.
+cudaError_t fault_word_for_launch(unsigned **err) {
+#ifdef MSDA_CHECKED
+    return fault_word_address(err);
+#else
+    *err = nullptr;
+    return cudaSuccess;
+#endif
+}
+
+}  // namespace msda
+
+extern "C" {
+
+int msda_checked_build(void) {
+#ifdef MSDA_CHECKED
+    return 1;
+#else
+    return 0;
+#endif
+}
+
+msda_status_t msda_device_check(void *stream) {
+    if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return MSDA_ERR_CUDA;
+#ifdef MSDA_CHECKED
+    unsigned *word = nullptr;
+    if (msda::fault_word_address(&word) != cudaSuccess) return MSDA_ERR_CUDA;
+    unsigned v = 0u;
+    if (cudaMemcpy(&v, word, sizeof v, cudaMemcpyDeviceToHost) != cudaSuccess) return MSDA_ERR_CUDA;
+    if (v != 0u) {
+        const unsigned zero = 0u;
+        if (cudaMemcpy(word, &zero, sizeof zero, cudaMemcpyHostToDevice) != cudaSuccess)
+            return MSDA_ERR_CUDA;
+        return MSDA_ERR_DEVICE_BOUNDS;
+    }
+#endif
+    return MSDA_OK;
+}
+
+msda_status_t msda_debug_bounds_self_test(void *stream) {
+    msda::Params p = {};
+    if (msda::fault_word_for_launch(&p.err) != cudaSuccess) return MSDA_ERR_CUDA;
+    msda::bounds_self_test_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(p);
+    return cudaGetLastError() == cudaSuccess ? MSDA_OK : MSDA_ERR_CUDA;
+}
+
+}  // extern "C"

@@ -37,7 +37,38 @@ struct Params {
     int MD;                // M*D elements per value row
     float inv_K;           // 1/K, for level = floor((idx + 0.5) / K)
     int64_t triples;       // B*Q*M
+    unsigned *err;         // checked build: device word of range faults (see in_tensor)
 };
+
+// ------------------------------------------------------------ checked build
+// Built with -DMSDA_CHECKED (libmsda_checked.so), every global access of the
+// kernels is first checked against the extent of the tensor it belongs to:
+// an access that would leave it is skipped (a load yields zeros) and bit 0 of
+// the device word p.err is set, which msda_device_check reads and clears.
+// No access is ever made outside a tensor and nothing traps. In the normal
+// build the check is the constant true and compiles away.
+#ifdef MSDA_CHECKED
+template <typename E>
+__device__ __forceinline__ bool in_tensor(const Params &p, const E *base, const E *at, int64_t n,
+                                          int64_t extent) {
+    const int64_t off = at - base;
+    const bool ok = base != nullptr && off >= 0 && n >= 0 && off <= extent - n;
+    if (!ok && p.err) atomicOr(p.err, 1u);
+    return ok;
+}
+#else
+template <typename E>
+__device__ __forceinline__ constexpr bool in_tensor(const Params &, const E *, const E *, int64_t,
+                                                    int64_t) {
+    return true;
+}
+#endif
+// element counts of the tensors the kernels touch
+__device__ __forceinline__ int64_t n_value(const Params &p) {
+    return (int64_t)p.B * p.S * p.M * p.D;
+}
+__device__ __forceinline__ int64_t n_samples(const Params &p) { return p.triples * p.LK; }
+__device__ __forceinline__ int64_t n_out(const Params &p) { return p.triples * p.D; }
 
 // Level table in shared memory. An invalid level gets W = H = -2 so that the
 // range test of every sample in it fails.
@@ -271,7 +302,7 @@ __device__ __forceinline__ Triple triple_of(int64_t t, const Params &p) {
     const int64_t rem = t - (int64_t)r.b * QM;
     const int qs = (int)(rem / p.M);
     r.m = (int)(rem - (int64_t)qs * p.M);
-    r.q = p.order ? p.order[qs] : qs;
+    r.q = p.order ? (in_tensor(p, p.order, p.order + qs, 1, p.Q) ? p.order[qs] : -1) : qs;
     r.bqm = ((int64_t)r.b * p.Q + r.q) * p.M + r.m;
     return r;
 }

@@ -17,6 +17,8 @@ msda_corners_kernel(const Params p, int32_t *rows) {
          s += (int64_t)gridDim.x * blockDim.x) {
         const int idx = (int)(s % p.LK);
         const int l = level_of(idx, p.inv_K);
+        if (!in_tensor(p, loc, loc + 2 * s, 2, 2 * n) || !in_tensor(p, rows, rows + 4 * s, 4, 4 * n))
+            continue;
         const float2 xy = load_xy<T>(loc + 2 * s);
         SampleGeom g;
         sample_geometry(g, xy.x, xy.y, lt, l);

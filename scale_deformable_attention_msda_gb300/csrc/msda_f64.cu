@@ -72,10 +72,16 @@ __global__ void __launch_bounds__(kThreads) msda_forward_f64_kernel(const Params
     bool valid;
     const Triple tr = group_triple(p, t, valid);
     if (!valid) return;   // no shuffles below: lanes may leave independently
-    const double *loc = reinterpret_cast<const double *>(p.loc) + tr.bqm * p.LK * 2;
-    const double *attn = reinterpret_cast<const double *>(p.attn) + tr.bqm * p.LK;
-    const double *vbase = reinterpret_cast<const double *>(p.value) +
-                          ((int64_t)tr.b * p.S * p.M + tr.m) * p.D + 2 * r;
+    const double *loc0 = reinterpret_cast<const double *>(p.loc);
+    const double *attn0 = reinterpret_cast<const double *>(p.attn);
+    const double *value = reinterpret_cast<const double *>(p.value);
+    const double *loc = loc0 + tr.bqm * p.LK * 2;
+    const double *attn = attn0 + tr.bqm * p.LK;
+    const double *vbase = value + ((int64_t)tr.b * p.S * p.M + tr.m) * p.D + 2 * r;
+    const int64_t nv = n_value(p), ns = n_samples(p);
+    if (!in_tensor(p, loc0, loc, 2 * (int64_t)p.LK, 2 * ns) ||
+        !in_tensor(p, attn0, attn, p.LK, ns))
+        return;
     double mx = 0.0, inv = 1.0;
     if (SOFTMAX) softmax64(attn, p.LK, mx, inv);
     double acc0 = 0.0, acc1 = 0.0;
@@ -89,15 +95,16 @@ __global__ void __launch_bounds__(kThreads) msda_forward_f64_kernel(const Params
                              (g.vx0 && g.vy1) ? a * hx * g.ly : 0.0, (g.vx1 && g.vy1) ? a * g.lx * g.ly : 0.0};
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
-            if (w[c] != 0.0) {
+            if (w[c] != 0.0 && in_tensor(p, value, vbase + (int64_t)g.row[c] * p.MD, 2, nv)) {
                 const double2 v = __ldg(reinterpret_cast<const double2 *>(vbase + (int64_t)g.row[c] * p.MD));
                 acc0 = fma(w[c], v.x, acc0);
                 acc1 = fma(w[c], v.y, acc1);
             }
         }
     }
-    double *o = reinterpret_cast<double *>(p.out) + tr.bqm * p.D + 2 * r;
-    *reinterpret_cast<double2 *>(o) = make_double2(acc0, acc1);
+    double *out = reinterpret_cast<double *>(p.out);
+    double *o = out + tr.bqm * p.D + 2 * r;
+    if (in_tensor(p, out, o, 2, n_out(p))) *reinterpret_cast<double2 *>(o) = make_double2(acc0, acc1);
 }
 
 __device__ __forceinline__ void red_add_f64(double *p, double v) {
@@ -116,19 +123,33 @@ __global__ void __launch_bounds__(kThreads) msda_backward_f64_kernel(const Param
     const int64_t t = ((int64_t)blockIdx.x * kThreads + threadIdx.x) / LPG;
     if (((int64_t)blockIdx.x * kThreads + (threadIdx.x & ~31)) / LPG >= p.triples) return;  // whole warp
     bool valid;
-    const Triple tr = group_triple(p, t, valid);
+    Triple tr = group_triple(p, t, valid);
     const int64_t bqm = valid ? tr.bqm : 0;
-    const double *loc = reinterpret_cast<const double *>(p.loc) + bqm * p.LK * 2;
-    const double *attn = reinterpret_cast<const double *>(p.attn) + bqm * p.LK;
+    const double *loc0 = reinterpret_cast<const double *>(p.loc);
+    const double *attn0 = reinterpret_cast<const double *>(p.attn);
+    const double *value = reinterpret_cast<const double *>(p.value);
+    double *gv0 = reinterpret_cast<double *>(p.grad_value);
+    double *gloc0 = reinterpret_cast<double *>(p.grad_loc);
+    double *gattn0 = reinterpret_cast<double *>(p.grad_attn);
+    const double *gout = reinterpret_cast<const double *>(p.grad_out);
+    const double *loc = loc0 + bqm * p.LK * 2;
+    const double *attn = attn0 + bqm * p.LK;
     const int64_t head = ((int64_t)tr.b * p.S * p.M + tr.m) * p.D + 2 * r;
-    const double *vbase = reinterpret_cast<const double *>(p.value) + head;
-    double *gvbase = reinterpret_cast<double *>(p.grad_value) + head;
-    double *gloc = reinterpret_cast<double *>(p.grad_loc) + bqm * p.LK * 2;
-    double *gattn = reinterpret_cast<double *>(p.grad_attn) + bqm * p.LK;
+    const double *vbase = value + head;
+    double *gvbase = gv0 + head;
+    double *gloc = gloc0 + bqm * p.LK * 2;
+    double *gattn = gattn0 + bqm * p.LK;
+    const int64_t nv = n_value(p), ns = n_samples(p);
+    // a group's per-sample rows are contiguous blocks of L*K entries
+    if (valid && (!in_tensor(p, loc0, loc, 2 * (int64_t)p.LK, 2 * ns) ||
+                  !in_tensor(p, attn0, attn, p.LK, ns) ||
+                  !in_tensor(p, gloc0, gloc, 2 * (int64_t)p.LK, 2 * ns) ||
+                  !in_tensor(p, gattn0, gattn, p.LK, ns) ||
+                  !in_tensor(p, gout, gout + tr.bqm * p.D + 2 * r, 2, n_out(p))))
+        valid = false;
     double g0 = 0.0, g1 = 0.0;
     if (valid) {
-        const double2 g = __ldg(reinterpret_cast<const double2 *>(
-            reinterpret_cast<const double *>(p.grad_out) + tr.bqm * p.D + 2 * r));
+        const double2 g = __ldg(reinterpret_cast<const double2 *>(gout + tr.bqm * p.D + 2 * r));
         g0 = g.x;
         g1 = g.y;
     }
@@ -149,7 +170,9 @@ __global__ void __launch_bounds__(kThreads) msda_backward_f64_kernel(const Param
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
             s[c] = 0.0;
-            if (vc[c]) {
+            if (vc[c] && in_tensor(p, value, vbase + (int64_t)g.row[c] * p.MD, 2, nv) &&
+                in_tensor(p, (const double *)gv0, (const double *)gvbase + (int64_t)g.row[c] * p.MD,
+                          2, nv)) {
                 const int64_t off = (int64_t)g.row[c] * p.MD;
                 const double2 v = __ldg(reinterpret_cast<const double2 *>(vbase + off));
                 s[c] = fma(g0, v.x, g1 * v.y);
@@ -193,6 +216,8 @@ __global__ void __launch_bounds__(kThreads) msda_corners_f64_kernel(const Params
     for (int64_t s = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; s < n;
          s += (int64_t)gridDim.x * blockDim.x) {
         const int l = level_of((int)(s % p.LK), p.inv_K);
+        if (!in_tensor(p, loc, loc + 2 * s, 2, 2 * n) || !in_tensor(p, rows, rows + 4 * s, 4, 4 * n))
+            continue;
         Geom64 g;
         sample_geometry64(g, loc[2 * s], loc[2 * s + 1], lt, l);
         reinterpret_cast<int4 *>(rows)[s] =

@@ -49,8 +49,9 @@ msda_forward_kernel(const Params p) {
     const bool active = t < p.triples;
     Triple tr = triple_of(active ? t : t0, p);
     const bool valid_q = active && tr.q >= 0 && tr.q < p.Q;
-    const T *vbase = reinterpret_cast<const T *>(p.value) +
-                     ((int64_t)tr.b * p.S * p.M + tr.m) * p.D + r * VEC;
+    const T *value = reinterpret_cast<const T *>(p.value);
+    const T *vbase = value + ((int64_t)tr.b * p.S * p.M + tr.m) * p.D + r * VEC;
+    const int64_t nv = n_value(p), ns = n_samples(p);
 
     // Phase 1 fills descriptor slot lane + 32*i, stored in [sample][group]
     // order, so consecutive lanes write consecutive 16-byte words (no bank
@@ -68,7 +69,8 @@ msda_forward_kernel(const Params p) {
     // With SOFTMAX, attn holds logits: the weight of sample idx is
     // exp(logit - max) / sum over the L*K logits of the prepared query-head.
     SoftmaxStats sm = {0.0f, 1.0f};
-    if (SOFTMAX) sm = softmax_stats<T, LPG>(attn + trp.bqm * p.LK, prep_ok ? p.LK : 0, lane);
+    const bool logits_ok = prep_ok && in_tensor(p, attn, attn + trp.bqm * p.LK, p.LK, ns);
+    if (SOFTMAX) sm = softmax_stats<T, LPG>(attn + trp.bqm * p.LK, logits_ok ? p.LK : 0, lane);
 
     float acc[VEC];
 #pragma unroll
@@ -84,9 +86,11 @@ msda_forward_kernel(const Params p) {
             int4 o = make_int4(0, 0, 0, 0);
             if (prep_ok && idx < p.LK) {
                 const int64_t e = trp.bqm * p.LK + idx;
-                const float2 xy = load_xy<T>(loc + 2 * e);
-                const float a = SOFTMAX ? softmax_weight(load_scalar<T>(attn + e), sm)
-                                        : load_scalar<T>(attn + e);
+                const float2 xy = in_tensor(p, loc, loc + 2 * e, 2, 2 * ns)
+                                      ? load_xy<T>(loc + 2 * e) : make_float2(0.f, 0.f);
+                const float z = in_tensor(p, attn, attn + e, 1, ns) ? load_scalar<T>(attn + e)
+                                                                     : 0.0f;
+                const float a = SOFTMAX ? softmax_weight(z, sm) : z;
                 const int l = level_of(idx, p.inv_K);
                 SampleGeom sg;
                 sample_geometry(sg, xy.x, xy.y, lt, l);
@@ -113,10 +117,11 @@ msda_forward_kernel(const Params p) {
             for (int u = 0; u < U; ++u) {
                 w[u] = s_w[warp][(j + u) * GPW + g];
                 const int4 o = s_o[warp][(j + u) * GPW + g];
-                v[u][0] = ldg16(vbase + o.x);
-                v[u][1] = ldg16(vbase + o.y);
-                v[u][2] = ldg16(vbase + o.z);
-                v[u][3] = ldg16(vbase + o.w);
+                const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
+                v[u][0] = in_tensor(p, value, vbase + o.x, VEC, nv) ? ldg16(vbase + o.x) : zero;
+                v[u][1] = in_tensor(p, value, vbase + o.y, VEC, nv) ? ldg16(vbase + o.y) : zero;
+                v[u][2] = in_tensor(p, value, vbase + o.z, VEC, nv) ? ldg16(vbase + o.z) : zero;
+                v[u][3] = in_tensor(p, value, vbase + o.w, VEC, nv) ? ldg16(vbase + o.w) : zero;
             }
 #pragma unroll
             for (int u = 0; u < U; ++u) {
@@ -130,8 +135,9 @@ msda_forward_kernel(const Params p) {
     }
 
     if (valid_q) {
-        T *o = reinterpret_cast<T *>(p.out) + tr.bqm * p.D + r * VEC;
-        *reinterpret_cast<uint4 *>(o) = pack16<T>(acc);
+        T *out = reinterpret_cast<T *>(p.out);
+        T *o = out + tr.bqm * p.D + r * VEC;
+        if (in_tensor(p, out, o, VEC, n_out(p))) *reinterpret_cast<uint4 *>(o) = pack16<T>(acc);
     }
 }
 

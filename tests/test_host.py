@@ -45,14 +45,23 @@ def test_library_exports_every_declared_symbol(so):
 def test_library_exports_nothing_else(so):
     import subprocess
     from scale_deformable_attention_msda_gb300 import build
-    out = subprocess.run(["nm", "-D", "--defined-only", build.LIBRARY], capture_output=True,
-                         text=True, check=True).stdout
-    exported = {line.split()[-1] for line in out.splitlines() if " T " in line}
-    assert exported == set(_declared_symbols())
+    for lib in (build.LIBRARY, build.CHECKED_LIBRARY):
+        out = subprocess.run(["nm", "-D", "--defined-only", lib], capture_output=True,
+                             text=True, check=True).stdout
+        exported = {line.split()[-1] for line in out.splitlines() if " T " in line}
+        assert exported == set(_declared_symbols()), lib
+
+
+def test_checked_build_flag(so):
+    """libmsda.so is the plain build, libmsda_checked.so the range-checked one
+    (the flag is a constant: no CUDA call)."""
+    from scale_deformable_attention_msda_gb300 import binding, build
+    assert so.msda_checked_build() == 0
+    assert binding.load(build.CHECKED_LIBRARY).msda_checked_build() == 1
 
 
 def test_status_strings_and_version(so):
-    for s in range(7):
+    for s in range(8):
         assert so.msda_status_string(s)
     assert so.msda_status_string(99) == b"unknown status"
     assert so.msda_version() >= 100
