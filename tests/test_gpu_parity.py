@@ -102,6 +102,7 @@ def check(got, ref, dtype, label=""):
 def run_and_check(w, accum=FP32BUF, order=None, label=None):
     p = wl.make_inputs(w)
     got = gpu_run(p, w.dtype, accum, order)
+    assert binding.msda_device_check() == 0      # no fault recorded by any kernel
     ref = oracle_run(p)
     return check(got, ref, w.dtype, label or w.name)
 
