@@ -62,7 +62,8 @@ def parse_args(argv=None):
     ap.add_argument("--configs", action="store_true",
                     help="instead of the benchmark line, time forward and backward (cold "
                          "and warm L2) on the decoder, encoder and Mask2Former "
-                         "configurations, with the fp64 oracle on 1 thread and all cores, "
+                         "configurations and the sweep point Q=5000, K=4, L=4, with the "
+                         "fp64 oracle on 1 thread and all cores, "
                          "one JSON line per configuration")
     a = ap.parse_args(argv)
     if a.warmup < 3:
@@ -609,7 +610,8 @@ def run_configs(args):
     plan = [(wl.decoder, "f32", "fp32_buffer"), (wl.decoder, "bf16", "fp32_buffer"),
             (wl.encoder, "f32", "fp32_buffer"), (wl.encoder, "bf16", "fp32_buffer"),
             (wl.encoder, "bf16", "native"), (wl.mask2former, "bf16", "fp32_buffer"),
-            (wl.mask2former, "bf16", "native")]
+            (wl.mask2former, "bf16", "native"),
+            (lambda dt: wl.sweep(5000, 4, 4, dtype=dt), "bf16", "fp32_buffer")]
     for make, dtype, acc_name in plan:
         w = make(dtype)
         p = wl.make_inputs(w)
