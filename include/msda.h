@@ -275,6 +275,19 @@ MSDA_API int msda_checked_build(void);
 MSDA_API msda_status_t msda_device_check(void *stream);
 MSDA_API msda_status_t msda_debug_bounds_self_test(void *stream);
 
+/* Sample split (launch tuning; process-wide). With one lane group per
+ * (b, q, m), a problem with few query-heads -- a detector decoder's B*Q*M =
+ * 4,800 -- occupies a fraction of the SMs. The kernels then spread each
+ * query-head's L*K samples over 2^s lane groups of one warp, which combine
+ * their partial results with warp shuffles. Results agree with s = 0 up to
+ * the fp32 summation order. By default (log2_groups = -1) s is chosen per
+ * launch from the problem size; 0 to 3 force s, clamped per launch to the
+ * groups of a warp and to L*K. Applies to the 16-bit and fp32 kernels (fp64
+ * kernels never split). Meant for tests and tuning: set it when no other
+ * thread is launching. MSDA_ERR_SHAPE for a value outside -1..3, which
+ * leaves the setting unchanged. */
+MSDA_API msda_status_t msda_set_sample_split(int log2_groups);
+
 /* Static description of a status code (never NULL). */
 MSDA_API const char *msda_status_string(msda_status_t status);
 

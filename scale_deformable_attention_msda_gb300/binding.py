@@ -28,7 +28,8 @@ EXPORTED = ("msda_forward", "msda_backward_workspace_bytes", "msda_backward",
             "msda_backward_zero", "msda_backward_accumulate", "msda_backward_finish",
             "msda_backward_static_workspace", "msda_forward_softmax", "msda_backward_softmax",
             "msda_debug_corners", "msda_checked_build", "msda_device_check",
-            "msda_debug_bounds_self_test", "msda_status_string", "msda_version")
+            "msda_debug_bounds_self_test", "msda_set_sample_split", "msda_status_string",
+            "msda_version")
 
 
 class msda_dims_t(ctypes.Structure):
@@ -88,6 +89,8 @@ def load(path: str | None = None):
     so.msda_device_check.restype = ctypes.c_int
     so.msda_debug_bounds_self_test.argtypes = [vp]
     so.msda_debug_bounds_self_test.restype = ctypes.c_int
+    so.msda_set_sample_split.argtypes = [ctypes.c_int]
+    so.msda_set_sample_split.restype = ctypes.c_int
     so.msda_status_string.argtypes = [ctypes.c_int]
     so.msda_status_string.restype = ctypes.c_char_p
     so.msda_version.argtypes = []
@@ -259,6 +262,13 @@ def msda_device_check(stream=None) -> int:
     if st not in (0, MSDA_ERR_DEVICE_BOUNDS):
         raise MSDAError(st, "msda_device_check")
     return st
+
+
+def msda_set_sample_split(log2_groups: int = -1):
+    """Process-wide sample split of the 16-bit and fp32 kernels: -1 (the
+    default) chooses it per launch from the problem size, 0..3 force 2^s lane
+    groups per query-head (clamped per launch). For tests and tuning."""
+    _call("msda_set_sample_split", lib().msda_set_sample_split(int(log2_groups)))
 
 
 def msda_debug_bounds_self_test(stream=None):

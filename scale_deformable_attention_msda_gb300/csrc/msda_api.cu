@@ -2,6 +2,8 @@
 // The entry points and their contracts are declared in include/msda.h.
 #include <stdint.h>
 
+#include <atomic>
+
 #include "msda_common.cuh"
 
 namespace msda {
@@ -61,8 +63,12 @@ msda_status_t check_dims(const msda_dims_t *d, msda_dtype_t dt, int *lpg) {
     return MSDA_OK;
 }
 
+// msda_set_sample_split: -1 chooses the split per launch, 0..3 force it.
+std::atomic<int> g_sample_split{-1};
+
 Params make_params(const msda_dims_t &d) {
     Params p = {};
+    p.split_log2 = g_sample_split.load(std::memory_order_relaxed);
     p.B = (int)d.B;
     p.S = (int)d.S;
     p.Q = (int)d.Q;
@@ -106,6 +112,12 @@ msda_status_t check_common(const void *value, const int64_t *shapes, const int64
 extern "C" {
 
 int msda_version(void) { return 100; }
+
+msda_status_t msda_set_sample_split(int log2_groups) {
+    if (log2_groups < -1 || log2_groups > 3) return MSDA_ERR_SHAPE;
+    g_sample_split.store(log2_groups, std::memory_order_relaxed);
+    return MSDA_OK;
+}
 
 const char *msda_status_string(msda_status_t s) {
     switch (s) {

@@ -19,11 +19,17 @@
 //     broadcast) and issues four 16-byte loads per sample, U samples at a
 //     time so that 4U loads are in flight, accumulating in fp32 registers.
 // The group then writes its D output channels once (16 bytes per lane).
+//
+// SPL (small problems, see choose_split): 2^s groups of a warp share one
+// query-head, each gathering every 2^s-th of its samples, and reduce their
+// partial sums with xor shuffles across the group bits of the lane index
+// before the first of them writes the output (a warp-level reduction across
+// the L x K samples).
 #include "msda_common.cuh"
 
 namespace msda {
 
-template <typename T, int LPG, bool SOFTMAX>
+template <typename T, int LPG, bool SOFTMAX, bool SPL>
 __global__ void __launch_bounds__(kThreads)
 msda_forward_kernel(const Params p) {
     constexpr int VEC = Vec16<T>::N;
@@ -41,11 +47,14 @@ msda_forward_kernel(const Params p) {
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g = lane / LPG, r = lane % LPG;
-    const int64_t t0 = ((int64_t)blockIdx.x * kWarpsPerBlock + warp) * GPW;
+    // sl2: log2 of the groups per query-head (0 unless SPL)
+    const int sl2 = SPL ? p.split_log2 : 0;
+    const int64_t t0 = ((int64_t)blockIdx.x * kWarpsPerBlock + warp) * (GPW >> sl2);
     if (t0 >= p.triples) return;
 
-    // this lane's group
-    const int64_t t = t0 + g;
+    // this lane's group: query-head t0 + (g >> sl2), sample subset sub
+    const int sub = g & ((1 << sl2) - 1);
+    const int64_t t = t0 + (g >> sl2);
     const bool active = t < p.triples;
     Triple tr = triple_of(active ? t : t0, p);
     const bool valid_q = active && tr.q >= 0 && tr.q < p.Q;
@@ -57,8 +66,11 @@ msda_forward_kernel(const Params p) {
     // order, so consecutive lanes write consecutive 16-byte words (no bank
     // conflicts). Slot lane + 32*i belongs to group lane % GPW and sample
     // lane / GPW + i*LPG of the chunk: each lane prepares one triple's samples.
+    // With a split, group pg's chunk sample j is sample (j << sl2) + psub of
+    // its query-head's chunk.
     const int pg = lane % GPW, pj = lane / GPW;
-    const int64_t tp = t0 + pg;
+    const int psub = pg & ((1 << sl2) - 1);
+    const int64_t tp = t0 + (pg >> sl2);
     bool prep_ok = tp < p.triples;
     const Triple trp = triple_of(prep_ok ? tp : t0, p);
     prep_ok = prep_ok && trp.q >= 0 && trp.q < p.Q;
@@ -70,18 +82,18 @@ msda_forward_kernel(const Params p) {
     // exp(logit - max) / sum over the L*K logits of the prepared query-head.
     SoftmaxStats sm = {0.0f, 1.0f};
     const bool logits_ok = prep_ok && in_tensor(p, attn, attn + trp.bqm * p.LK, p.LK, ns);
-    if (SOFTMAX) sm = softmax_stats<T, LPG>(attn + trp.bqm * p.LK, logits_ok ? p.LK : 0, lane);
+    if (SOFTMAX) sm = softmax_stats<T, LPG>(attn + trp.bqm * p.LK, logits_ok ? p.LK : 0, lane, sl2);
 
     float acc[VEC];
 #pragma unroll
     for (int i = 0; i < VEC; ++i) acc[i] = 0.0f;
 
-    for (int base = 0; base < p.LK; base += CH) {
+    for (int base = 0; base < p.LK; base += CH << sl2) {
         // ---- phase 1: descriptors
 #pragma unroll
         for (int i = 0; i < SPW / 32; ++i) {
             const int j = pj + i * LPG;
-            const int idx = base + j;
+            const int idx = base + (j << sl2) + psub;
             float4 w = make_float4(0.f, 0.f, 0.f, 0.f);
             int4 o = make_int4(0, 0, 0, 0);
             if (prep_ok && idx < p.LK) {
@@ -109,7 +121,7 @@ msda_forward_kernel(const Params p) {
         __syncwarp();
 
         // ---- phase 2: gather
-        const int n = min(CH, p.LK - base);
+        const int n = min(CH, (p.LK - base + (1 << sl2) - 1) >> sl2);
         for (int j = 0; j < n; j += U) {
             float4 w[U];
             uint4 v[U][4];
@@ -118,6 +130,10 @@ msda_forward_kernel(const Params p) {
                 w[u] = s_w[warp][(j + u) * GPW + g];
                 const int4 o = s_o[warp][(j + u) * GPW + g];
                 const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
+                if (SPL && j + u >= n) {   // a split group's chunk is mostly empty slots
+                    v[u][0] = v[u][1] = v[u][2] = v[u][3] = zero;
+                    continue;
+                }
                 v[u][0] = in_tensor(p, value, vbase + o.x, VEC, nv) ? ldg16(vbase + o.x) : zero;
                 v[u][1] = in_tensor(p, value, vbase + o.y, VEC, nv) ? ldg16(vbase + o.y) : zero;
                 v[u][2] = in_tensor(p, value, vbase + o.z, VEC, nv) ? ldg16(vbase + o.z) : zero;
@@ -134,45 +150,57 @@ msda_forward_kernel(const Params p) {
         __syncwarp();
     }
 
-    if (valid_q) {
+    if (SPL) {
+        for (int off = LPG; off < (LPG << sl2); off <<= 1) {
+#pragma unroll
+            for (int i = 0; i < VEC; ++i) acc[i] += __shfl_xor_sync(0xffffffffu, acc[i], off);
+        }
+    }
+    if (valid_q && sub == 0) {
         T *out = reinterpret_cast<T *>(p.out);
         T *o = out + tr.bqm * p.D + r * VEC;
         if (in_tensor(p, out, o, VEC, n_out(p))) *reinterpret_cast<uint4 *>(o) = pack16<T>(acc);
     }
 }
 
-template <typename T, bool SOFTMAX>
+template <typename T, bool SOFTMAX, bool SPL>
 static cudaError_t launch_forward_t(const Params &p, int lpg, cudaStream_t stream) {
     const int gpw = 32 / lpg;
-    const int64_t warps = (p.triples + gpw - 1) / gpw;
+    const int64_t per_warp = gpw >> p.split_log2;     // query-heads per warp
+    const int64_t warps = (p.triples + per_warp - 1) / per_warp;
     const int64_t blocks = (warps + kWarpsPerBlock - 1) / kWarpsPerBlock;
     if (blocks == 0) return cudaSuccess;
     if (blocks > 0x7fffffff) return cudaErrorInvalidConfiguration;
     const dim3 grid((unsigned)blocks);
     switch (lpg) {
-        case 1: msda_forward_kernel<T, 1, SOFTMAX><<<grid, kThreads, 0, stream>>>(p); break;
-        case 2: msda_forward_kernel<T, 2, SOFTMAX><<<grid, kThreads, 0, stream>>>(p); break;
-        case 4: msda_forward_kernel<T, 4, SOFTMAX><<<grid, kThreads, 0, stream>>>(p); break;
-        case 8: msda_forward_kernel<T, 8, SOFTMAX><<<grid, kThreads, 0, stream>>>(p); break;
-        case 16: msda_forward_kernel<T, 16, SOFTMAX><<<grid, kThreads, 0, stream>>>(p); break;
-        case 32: msda_forward_kernel<T, 32, SOFTMAX><<<grid, kThreads, 0, stream>>>(p); break;
+        case 1: msda_forward_kernel<T, 1, SOFTMAX, SPL><<<grid, kThreads, 0, stream>>>(p); break;
+        case 2: msda_forward_kernel<T, 2, SOFTMAX, SPL><<<grid, kThreads, 0, stream>>>(p); break;
+        case 4: msda_forward_kernel<T, 4, SOFTMAX, SPL><<<grid, kThreads, 0, stream>>>(p); break;
+        case 8: msda_forward_kernel<T, 8, SOFTMAX, SPL><<<grid, kThreads, 0, stream>>>(p); break;
+        case 16: msda_forward_kernel<T, 16, SOFTMAX, SPL><<<grid, kThreads, 0, stream>>>(p); break;
+        case 32: msda_forward_kernel<T, 32, SOFTMAX, SPL><<<grid, kThreads, 0, stream>>>(p); break;
         default: return cudaErrorInvalidValue;
     }
     return cudaGetLastError();
 }
 
+template <typename T>
+static cudaError_t launch_forward_d(const Params &p0, int lpg, bool softmax, cudaStream_t stream) {
+    Params p = p0;
+    p.split_log2 = choose_split(p.triples, 32 / lpg, p.LK, p0.split_log2);
+    if (p.split_log2 > 0)
+        return softmax ? launch_forward_t<T, true, true>(p, lpg, stream)
+                       : launch_forward_t<T, false, true>(p, lpg, stream);
+    return softmax ? launch_forward_t<T, true, false>(p, lpg, stream)
+                   : launch_forward_t<T, false, false>(p, lpg, stream);
+}
+
 cudaError_t launch_forward(const Params &p, msda_dtype_t dt, int lpg, bool softmax,
                            cudaStream_t stream) {
     switch (dt) {
-        case MSDA_F32:
-            return softmax ? launch_forward_t<float, true>(p, lpg, stream)
-                           : launch_forward_t<float, false>(p, lpg, stream);
-        case MSDA_BF16:
-            return softmax ? launch_forward_t<__nv_bfloat16, true>(p, lpg, stream)
-                           : launch_forward_t<__nv_bfloat16, false>(p, lpg, stream);
-        case MSDA_F16:
-            return softmax ? launch_forward_t<__half, true>(p, lpg, stream)
-                           : launch_forward_t<__half, false>(p, lpg, stream);
+        case MSDA_F32: return launch_forward_d<float>(p, lpg, softmax, stream);
+        case MSDA_BF16: return launch_forward_d<__nv_bfloat16>(p, lpg, softmax, stream);
+        case MSDA_F16: return launch_forward_d<__half>(p, lpg, softmax, stream);
     }
     return cudaErrorInvalidValue;
 }

@@ -261,9 +261,47 @@ def test_channel_widths(dtype, D):
     run_and_check(_small(D=D, dtype=dtype, M=2), FP32BUF, label=f"D={D}")
 
 
+@pytest.fixture
+def sample_split(request):
+    """Force the kernels' sample split (2^s lane groups per query-head) for
+    one test, then restore the size-based choice."""
+    binding.msda_set_sample_split(request.param)
+    yield request.param
+    binding.msda_set_sample_split(-1)
+
+
+SPLITS = [-1, 0, 1, 3]      # automatic, off, two groups, eight groups (clamped)
+
+
+@pytest.mark.parametrize("sample_split", SPLITS, indirect=True)
 @pytest.mark.parametrize("Q", [1, 7, 31, 33, 129, 1001])
-def test_ragged_query_counts(Q):
-    run_and_check(_small(Q=Q, B=3), label=f"Q={Q}")
+def test_ragged_query_counts(Q, sample_split):
+    run_and_check(_small(Q=Q, B=3), label=f"Q={Q} split={sample_split}")
+
+
+@pytest.mark.parametrize("sample_split", SPLITS, indirect=True)
+@pytest.mark.parametrize("dtype,accum,D,K", [("f32", FP32BUF, 32, 4), ("bf16", FP32BUF, 32, 4),
+                                             ("bf16", NATIVE, 32, 4), ("f16", FP32BUF, 64, 3),
+                                             ("bf16", FP32BUF, 8, 5), ("f32", FP32BUF, 4, 2)])
+def test_sample_split_modes(dtype, accum, D, K, sample_split):
+    """Every split level on every lane mapping (16-byte and 8-byte lanes,
+    native and fp32 accumulation, one to 16 lanes per query-head), with
+    sample counts that do not divide the groups, plain and softmax."""
+    w = _small(Q=45, M=3, D=D, K=K, dtype=dtype)
+    run_and_check(w, accum, label=f"{dtype} D={D} K={K} split={sample_split}")
+    p = wl.make_inputs(w)
+    t = upload(p, w.dtype)
+    z = to_dev(p["logits"], w.dtype)
+    out = binding.msda_forward(t["value"], t["shapes"], t["starts"], t["loc"], z, softmax=True)
+    gv, gl, gz = binding.msda_backward(t["value"], t["shapes"], t["starts"], t["loc"], z,
+                                       t["grad_out"], softmax=True, accum=accum)
+    torch.cuda.synchronize()
+    got = {"out": np64(out), "gv": np64(gv), "gl": np64(gl), "ga": np64(gz)}
+    ref = {"out": oracle.forward_softmax(p["value"], p["shapes"], p["starts"], p["loc"],
+                                         p["logits"])}
+    ref["gv"], ref["gl"], ref["ga"] = oracle.backward_softmax(
+        p["value"], p["shapes"], p["starts"], p["loc"], p["logits"], p["grad_out"])
+    check(got, ref, w.dtype, f"softmax {dtype} D={D} K={K} split={sample_split}")
 
 
 @pytest.mark.parametrize("dtype,D,Q,M", [("f32", 32, 1, 3), ("f32", 32, 33, 5), ("bf16", 32, 7, 3),

@@ -67,6 +67,16 @@ def test_status_strings_and_version(so):
     assert so.msda_version() >= 100
 
 
+def test_sample_split_setting(so):
+    """-1..3 are accepted (no CUDA call); anything else is MSDA_ERR_SHAPE and
+    leaves the setting alone."""
+    for v in (0, 1, 2, 3, -1):
+        assert so.msda_set_sample_split(v) == 0
+    for v in (-2, 4, 99):
+        assert so.msda_set_sample_split(v) == 2
+    assert so.msda_set_sample_split(-1) == 0
+
+
 def _dims(**kw):
     from scale_deformable_attention_msda_gb300.binding import msda_dims_t
     d = dict(B=2, S=22223, Q=300, M=8, D=32, L=4, K=4)
