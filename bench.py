@@ -186,7 +186,7 @@ ACCUM_MODES = {"fp32_buffer": lambda b: b.MSDA_ACC_FP32_BUFFER,
                "native": lambda b: b.MSDA_ACC_NATIVE}
 
 KERNEL_SOURCES = {"msda_forward_kernel": ("msda_common.cuh", "msda_forward.cu"),
-                  "msda_backward_kernel": ("msda_common.cuh", "msda_backward.cu")}
+                  "msda_backward_kernel": ("msda_common.cuh", "msda_backward.cuh")}
 
 
 def kernel_source_hash(kernel: str) -> str:
