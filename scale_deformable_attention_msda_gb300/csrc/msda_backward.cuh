@@ -203,8 +203,13 @@ __device__ __forceinline__ void merge_shared_rows(float4 &w, const int4 &o, int 
 // whole 128-byte workspace row per query-head (L2 reduces 128-byte groups
 // about 1.2x faster than 64-byte ones); the extra per-lane work fits in the
 // kernel's idle issue slots.
+// Resident blocks per SM (GB300, encoder, measured): the narrow
+// instantiations are held to 4 (64 registers; the softmax one would take 74
+// and run at 3: 422.5 against 436.9 us), the others to 3 (at most 85
+// registers): native bf16 accumulation would take 96 and run at 2 blocks
+// (332 against 294 us), and the fp32 ones spill at 64.
 template <typename T, int LPG, bool F32ACC, bool SOFTMAX, bool NARROW, bool SPL>
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kThreads, NARROW ? 4 : 3)
 msda_backward_kernel(const Params p) {
     static_assert(!NARROW || (F32ACC && sizeof(T) == 2), "narrow lanes: 16-bit data, fp32 workspace");
     constexpr int LB = NARROW ? 8 : 16;      // bytes of one corner vector per lane
