@@ -205,11 +205,12 @@ __device__ __forceinline__ void merge_shared_rows(float4 &w, const int4 &o, int 
 // kernel's idle issue slots.
 // Resident blocks per SM (GB300, encoder, measured): the narrow
 // instantiations are held to 4 (64 registers; the softmax one would take 74
-// and run at 3: 422.5 against 436.9 us), the others to 3 (at most 85
-// registers): native bf16 accumulation would take 96 and run at 2 blocks
-// (332 against 294 us), and the fp32 ones spill at 64.
+// and run at 3: 422.5 against 436.9 us), and so are the fp32 ones, which
+// gather one sample at a time to fit (softmax 449 against 461 us, plain
+// unchanged); native 16-bit accumulation to 3 (80 registers; it would take
+// 96 and run at 2 blocks: 332 against 294 us).
 template <typename T, int LPG, bool F32ACC, bool SOFTMAX, bool NARROW, bool SPL>
-__global__ void __launch_bounds__(kThreads, NARROW ? 4 : 3)
+__global__ void __launch_bounds__(kThreads, (NARROW || sizeof(T) == 4) ? 4 : 3)
 msda_backward_kernel(const Params p) {
     static_assert(!NARROW || (F32ACC && sizeof(T) == 2), "narrow lanes: 16-bit data, fp32 workspace");
     constexpr int LB = NARROW ? 8 : 16;      // bytes of one corner vector per lane
@@ -218,7 +219,8 @@ msda_backward_kernel(const Params p) {
     constexpr int SPW = 64;
     constexpr int CH = SPW / GPW;
     constexpr int NP = SPW / 32;             // samples each lane prepares per chunk
-    constexpr int U = CH < 2 ? CH : 2;
+    constexpr int UW = (sizeof(T) == 4 && !NARROW) ? 1 : 2;   // samples gathered at a time
+    constexpr int U = CH < UW ? CH : UW;
     using S = Scatter<T, F32ACC, LPG>;
     using Acc = typename S::Acc;
     constexpr int NSC = NARROW ? VEC : S::NSC;
