@@ -203,14 +203,15 @@ __device__ __forceinline__ void merge_shared_rows(float4 &w, const int4 &o, int 
 // whole 128-byte workspace row per query-head (L2 reduces 128-byte groups
 // about 1.2x faster than 64-byte ones); the extra per-lane work fits in the
 // kernel's idle issue slots.
-// Resident blocks per SM (GB300, encoder, measured): the narrow
-// instantiations are held to 4 (64 registers; the softmax one would take 74
-// and run at 3: 422.5 against 436.9 us), and so are the fp32 ones, which
-// gather one sample at a time to fit (softmax 449 against 461 us, plain
-// unchanged); native 16-bit accumulation to 3 (80 registers; it would take
-// 96 and run at 2 blocks: 332 against 294 us).
+// Every instantiation is held to 4 resident blocks per SM (64 registers).
+// The narrow ones gather two samples at a time and fit; the 16-byte-lane
+// ones (fp32 data, native 16-bit adds) gather one at a time to fit. Measured
+// on the encoder (GB300): the narrow softmax backward would take 74
+// registers and run at 3 blocks (436.9 against 422.5 us); native bf16
+// accumulation took 96 registers at 2 blocks (332 us), 80 at 3 (291 us),
+// and takes 285 us here; the fp32 softmax one 461 against 449 us.
 template <typename T, int LPG, bool F32ACC, bool SOFTMAX, bool NARROW, bool SPL>
-__global__ void __launch_bounds__(kThreads, (NARROW || sizeof(T) == 4) ? 4 : 3)
+__global__ void __launch_bounds__(kThreads, 4)
 msda_backward_kernel(const Params p) {
     static_assert(!NARROW || (F32ACC && sizeof(T) == 2), "narrow lanes: 16-bit data, fp32 workspace");
     constexpr int LB = NARROW ? 8 : 16;      // bytes of one corner vector per lane
@@ -219,7 +220,7 @@ msda_backward_kernel(const Params p) {
     constexpr int SPW = 64;
     constexpr int CH = SPW / GPW;
     constexpr int NP = SPW / 32;             // samples each lane prepares per chunk
-    constexpr int UW = (sizeof(T) == 4 && !NARROW) ? 1 : 2;   // samples gathered at a time
+    constexpr int UW = NARROW ? 2 : 1;       // samples gathered at a time
     constexpr int U = CH < UW ? CH : UW;
     using S = Scatter<T, F32ACC, LPG>;
     using Acc = typename S::Acc;
