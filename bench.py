@@ -190,13 +190,19 @@ KERNEL_SOURCES = {"msda_forward_kernel": ("msda_common.cuh", "msda_forward.cu"),
 
 
 def kernel_source_hash(kernel: str) -> str:
-    """sha256 prefix of the source files that define `kernel`."""
+    """sha256 prefix of the code of the source files that define `kernel`:
+    comments and runs of whitespace are dropped first, so that editing a
+    comment does not retire the ncu counters taken on the same code."""
     import hashlib
+    import re
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "scale_deformable_attention_msda_gb300", "csrc")
     for name in KERNEL_SOURCES[kernel]:
+        text = open(os.path.join(csrc, name), encoding="utf-8").read()
+        text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", " ", text)
         h.update(name.encode())
-        h.update(open(os.path.join(csrc, name), "rb").read())
+        h.update(" ".join(text.split()).encode())
     return h.hexdigest()[:16]
 
 

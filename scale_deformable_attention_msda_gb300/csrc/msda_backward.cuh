@@ -10,12 +10,14 @@
 //   grad_loc_y = a H ((1-lx)(s_10 - s_00) + lx (s_11 - s_01))
 //
 // Work split as in the forward: a group of LPG lanes owns one (b,q,m), each
-// lane 16 bytes of its D channels. Per chunk of samples a warp
+// lane 16 bytes of its D channels (8 bytes in NARROW mode, below). Per chunk
+// of samples a warp
 //  1. prepares descriptors (lane per sample): corner rows, a*w_c for the
 //     scatter, and keeps lx, ly, a, W, H and the corner mask in registers;
-//  2. gathers (group per sample): four 16-byte corner loads, per-lane partial
-//     dot products with g, vector atomic adds of a*w_c*g into grad_value, and
-//     an xor-butterfly that completes the four dot products across the group;
+//  2. gathers (group per sample): four corner loads of the lane's bytes,
+//     per-lane partial dot products with g, vector atomic adds of a*w_c*g
+//     into grad_value, and an xor-butterfly that completes the four dot
+//     products across the group;
 //  3. finishes (lane per sample, the lane that prepared it): grad_attn and
 //     grad_loc from the four dot products, one coalesced store each.
 // No per-sample buffer exists outside shared memory (deformops README,
