@@ -189,19 +189,25 @@ def test_dispatch_order_changes_nothing(kind):
                                wl.sweep(5000, 8, 4), wl.decoder("f64")],
                          ids=lambda w: f"{w.name}-{w.dtype}")
 def test_softmax_variant(w):
+    _softmax_check(w, FP32BUF, f"softmax {w.name}")
+
+
+def _softmax_check(w, accum, label):
+    """The fused-softmax entry points on w's logits against the oracle's."""
     p = wl.make_inputs(w)
     t = upload(p, w.dtype)
     z = to_dev(p["logits"], w.dtype)
     out = binding.msda_forward(t["value"], t["shapes"], t["starts"], t["loc"], z, softmax=True)
     gv, gl, gz = binding.msda_backward(t["value"], t["shapes"], t["starts"], t["loc"], z,
-                                       t["grad_out"], softmax=True)
+                                       t["grad_out"], softmax=True, accum=accum)
     torch.cuda.synchronize()
+    assert binding.msda_device_check() == 0
     got = {"out": np64(out), "gv": np64(gv), "gl": np64(gl), "ga": np64(gz)}
     ref = {"out": oracle.forward_softmax(p["value"], p["shapes"], p["starts"], p["loc"],
                                          p["logits"])}
     ref["gv"], ref["gl"], ref["ga"] = oracle.backward_softmax(
         p["value"], p["shapes"], p["starts"], p["loc"], p["logits"], p["grad_out"])
-    check(got, ref, w.dtype, f"softmax {w.name}")
+    check(got, ref, w.dtype, label)
 
 
 # ------------------------------------------------------- integer parity
@@ -343,6 +349,28 @@ def test_grad_value_elementwise_bound(w):
                                       (5, tuple((2 + l, 3 + l) for l in range(16)))])
 def test_level_and_point_counts(K, levels):
     run_and_check(_small(K=K, levels=levels), label=f"K={K} L={len(levels)}")
+
+
+@pytest.mark.parametrize("sample_split", [-1, 3], indirect=True)
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_many_points_per_query_head(dtype, sample_split):
+    """K = 200 over three levels: 600 samples per query-head, so every group
+    walks many chunks of descriptors (and a split group takes every eighth
+    sample of a long list)."""
+    w = _small(B=2, Q=40, M=3, D=32, K=200, levels=((30, 40), (15, 20), (4, 5)), dtype=dtype,
+               sigma=4.0)
+    run_and_check(w, FP32BUF, label=f"K=200 {dtype} split={sample_split}")
+
+
+@pytest.mark.parametrize("dtype,D", [("bf16", 128), ("f32", 64)])
+def test_softmax_at_slot_capacity(dtype, D):
+    """The fused softmax keeps a warp's d loss / d weight in 512 shared
+    slots: L*K = 16 x (16-byte lanes per query-head) fills every slot of a
+    warp's query-heads (here 16 levels x 16 points)."""
+    levels = tuple((2 + l % 5, 3 + l % 4) for l in range(16))
+    w = _small(B=1, Q=20, M=3, D=D, K=16, levels=levels, dtype=dtype)
+    assert w.L * w.K == 16 * (D * (4 if dtype == "f32" else 2) // 16)
+    _softmax_check(w, FP32BUF, label=f"softmax at capacity {dtype} D={D}")
 
 
 def test_empty_problems():
