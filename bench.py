@@ -206,15 +206,29 @@ def kernel_source_hash(kernel: str) -> str:
     return h.hexdigest()[:16]
 
 
-def profiled_traffic(kernel: str):
+# The ncu summary that holds a kernel's counters for the bench's encoder run,
+# by (kernel, storage dtype, accumulator): each is a different instantiation,
+# and a run with no summary of its own reports no traffic.
+PROFILE_FILES = {
+    ("msda_forward_kernel", "bf16", "fp32_buffer"): "msda_forward_kernel_encoder.md",
+    ("msda_forward_kernel", "bf16", "native"): "msda_forward_kernel_encoder.md",
+    ("msda_backward_kernel", "bf16", "fp32_buffer"): "msda_backward_kernel_encoder.md",
+    ("msda_backward_kernel", "bf16", "native"): "msda_backward_kernel_native_encoder.md",
+}
+
+
+def profiled_traffic(kernel: str, dtype: str = "bf16", accum: str = "fp32_buffer"):
     """DRAM bytes per launch of `kernel` from the committed ncu summary, or None.
 
-    profiles/<kernel>_encoder.md carries a line
+    The summary (PROFILE_FILES) carries a line
     `traffic_bytes_per_launch: N  source_sha256: H`; the figure counts only
     while the kernel's sources still hash to H (else the kernel has changed
     since the counters were taken)."""
     import re
-    path = os.path.join(ROOT, "profiles", f"{kernel}_encoder.md")
+    name = PROFILE_FILES.get((kernel, dtype, accum))
+    if name is None:
+        return None
+    path = os.path.join(ROOT, "profiles", name)
     try:
         text = open(path).read()
     except OSError:
@@ -458,7 +472,7 @@ def run_ours(args):
     peak, peak_kind = measured_hbm_peak()
     kernel_name = {"forward": "msda_forward_kernel", "backward": "msda_backward_kernel"}
     achieved = algo[dominant] / (mean[dominant] * 1e-3) / 1e9
-    traffic = profiled_traffic(kernel_name[dominant])
+    traffic = profiled_traffic(kernel_name[dominant], args.dtype, args.accum)
     roofline = {"bound": "hbm", "kernel": kernel_name[dominant], "achieved": round(achieved, 1),
                 "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
                 "traffic": traffic, "algorithmic_bytes": algo[dominant],

@@ -60,6 +60,22 @@ def test_traffic_figure_needs_matching_kernel_sources(tmp_path):
     assert bench.profiled_traffic("no_such_kernel") is None
 
 
+def test_traffic_figure_belongs_to_the_instantiation_run():
+    """Each (kernel, dtype, accumulator) reads its own summary: the native
+    backward never reports the fp32-workspace kernel's DRAM bytes, and a run
+    with no summary (fp32 data) reports none. A comment edit keeps the hash."""
+    sys.path.insert(0, ROOT)
+    import bench
+    files = bench.PROFILE_FILES
+    assert files[("msda_backward_kernel", "bf16", "native")] != \
+        files[("msda_backward_kernel", "bf16", "fp32_buffer")]
+    for k in ("msda_forward_kernel", "msda_backward_kernel"):
+        assert bench.profiled_traffic(k, "f32", "fp32_buffer") is None
+        assert bench.profiled_traffic(k, "f16", "native") is None
+    for (k, _, _), name in files.items():
+        assert os.path.exists(os.path.join(ROOT, "profiles", name)), name
+
+
 def test_reference_arm_prints_its_line():
     r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
                         "--steps", "3", "--warmup", "3"], capture_output=True, text=True,
