@@ -214,6 +214,8 @@ PROFILE_FILES = {
     ("msda_forward_kernel", "bf16", "native"): "msda_forward_kernel_encoder.md",
     ("msda_backward_kernel", "bf16", "fp32_buffer"): "msda_backward_kernel_encoder.md",
     ("msda_backward_kernel", "bf16", "native"): "msda_backward_kernel_native_encoder.md",
+    ("msda_forward_kernel", "f32", "fp32_buffer"): "msda_kernels_f32_encoder.md",
+    ("msda_backward_kernel", "f32", "fp32_buffer"): "msda_kernels_f32_encoder.md",
 }
 
 
@@ -233,7 +235,10 @@ def profiled_traffic(kernel: str, dtype: str = "bf16", accum: str = "fp32_buffer
         text = open(path).read()
     except OSError:
         return None
-    m = re.search(r"traffic_bytes_per_launch:\s*(\d+)\s+source_sha256:\s*([0-9a-f]+)", text)
+    # a summary of several kernels qualifies each line with the kernel's name
+    m = (re.search(r"traffic_bytes_per_launch \(" + re.escape(kernel) +
+                   r"\):\s*(\d+)\s+source_sha256:\s*([0-9a-f]+)", text) or
+         re.search(r"traffic_bytes_per_launch:\s*(\d+)\s+source_sha256:\s*([0-9a-f]+)", text))
     if not m or kernel not in KERNEL_SOURCES:
         return None
     return int(m.group(1)) if m.group(2) == kernel_source_hash(kernel) else None

@@ -62,16 +62,20 @@ def test_traffic_figure_needs_matching_kernel_sources(tmp_path):
 
 def test_traffic_figure_belongs_to_the_instantiation_run():
     """Each (kernel, dtype, accumulator) reads its own summary: the native
-    backward never reports the fp32-workspace kernel's DRAM bytes, and a run
-    with no summary (fp32 data) reports none. A comment edit keeps the hash."""
+    backward never reports the fp32-workspace kernel's DRAM bytes, fp32 runs
+    read the fp32 kernels' lines of their shared summary, and a run with no
+    summary (fp16 data) reports none."""
     sys.path.insert(0, ROOT)
     import bench
     files = bench.PROFILE_FILES
     assert files[("msda_backward_kernel", "bf16", "native")] != \
         files[("msda_backward_kernel", "bf16", "fp32_buffer")]
     for k in ("msda_forward_kernel", "msda_backward_kernel"):
-        assert bench.profiled_traffic(k, "f32", "fp32_buffer") is None
         assert bench.profiled_traffic(k, "f16", "native") is None
+        f32 = bench.profiled_traffic(k, "f32", "fp32_buffer")
+        assert f32 is None or f32 != bench.profiled_traffic(k, "bf16", "fp32_buffer")
+    assert bench.profiled_traffic("msda_forward_kernel", "f32", "fp32_buffer") != \
+        bench.profiled_traffic("msda_backward_kernel", "f32", "fp32_buffer")
     for (k, _, _), name in files.items():
         assert os.path.exists(os.path.join(ROOT, "profiles", name)), name
 
