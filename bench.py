@@ -65,6 +65,10 @@ def parse_args(argv=None):
                          "configurations and the sweep point Q=5000, K=4, L=4, with the "
                          "fp64 oracle on 1 thread and all cores, "
                          "one JSON line per configuration")
+    ap.add_argument("--layer", action="store_true",
+                    help="instead of the benchmark line, time the MultiScaleDeformableAttention "
+                         "layer (projections + fused-softmax operator, bf16) forward and "
+                         "backward on the encoder shape, and the operator's share of it")
     a = ap.parse_args(argv)
     if a.warmup < 3:
         ap.error("--warmup must be at least 3")
@@ -762,8 +766,91 @@ def run_reference(args):
     return result
 
 
+def run_layer(args):
+    """The layer around the operator: MultiScaleDeformableAttention (dim 256,
+    8 heads, 4 levels, 4 points; its four projections are cuBLAS matmuls) in
+    bf16 on the encoder shape, forward + backward from a given output
+    gradient, L2 flushed before each step; and, on the same operands, the
+    operator alone (msda_forward_softmax + msda_backward_softmax)."""
+    import numpy as np
+    import torch
+
+    from scale_deformable_attention_msda_gb300 import binding, build, layer as lay, workloads as wl
+
+    build.build()
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    w = wl.encoder("bf16")
+    dim = w.M * w.D
+    rng = np.random.Generator(np.random.PCG64(77))
+    dt = torch.bfloat16
+    net = lay.MultiScaleDeformableAttention(dim, w.M, w.L, w.K).to(dev, dt)
+    query = torch.tensor(rng.standard_normal((w.B, w.Q, dim)), dtype=dt, device=dev).requires_grad_()
+    value = torch.tensor(rng.standard_normal((w.B, w.S, dim)), dtype=dt, device=dev).requires_grad_()
+    ref = torch.tensor(wl.reference_points(w, rng), dtype=torch.float32, device=dev)
+    shapes = torch.tensor(wl.spatial_shapes(w.levels), device=dev)
+    starts = torch.tensor(wl.level_start_index(w.levels), device=dev)
+    gout = torch.tensor(rng.standard_normal((w.B, w.Q, dim)), dtype=dt, device=dev)
+
+    def layer_step():
+        net.zero_grad(set_to_none=True)
+        query.grad = value.grad = None
+        net(query, ref, value, shapes, starts).backward(gout)
+
+    # the operator's operands, as the layer builds them
+    with torch.no_grad():
+        v = net.value_proj(value).view(w.B, w.S, w.M, w.D).contiguous()
+        off = net.sampling_offsets(query).view(w.B, w.Q, w.M, w.L, w.K, 2)
+        logits = net.attention_weights(query).view(w.B, w.Q, w.M, w.L, w.K).contiguous()
+        wh = shapes.flip(-1).to(off.dtype)
+        loc = (ref[:, :, None, None, None, :].to(off.dtype) +
+               off / wh[None, None, None, :, None, :]).contiguous()
+    g_op = torch.tensor(rng.standard_normal((w.B, w.Q, dim)), dtype=dt, device=dev)
+    buf = binding.BackwardBuffers(v, loc, logits, binding.MSDA_ACC_FP32_BUFFER)
+    out = torch.empty((w.B, w.Q, dim), dtype=dt, device=dev)
+
+    def op_step():
+        binding.msda_forward(v, shapes, starts, loc, logits, out=out, softmax=True)
+        binding.msda_backward(v, shapes, starts, loc, logits, g_op, softmax=True,
+                              grad_value=buf.grad_value,
+                              grad_sampling_locations=buf.grad_sampling_locations,
+                              grad_attention_weights=buf.grad_attention_weights,
+                              workspace=buf.workspace)
+
+    def timed(fn):
+        for _ in range(args.warmup):
+            fn()
+        ts = []
+        for i in range(min(args.steps, 200)):
+            flush.fill_(i & 255)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            fn()
+            e1.record()
+            torch.cuda.synchronize()
+            ts.append(e0.elapsed_time(e1))
+        ts.sort()
+        return ts[len(ts) // 2]
+
+    layer_ms, op_ms = timed(layer_step), timed(op_step)
+    print(json.dumps({
+        "mode": "layer", "workload": f"MultiScaleDeformableAttention(dim={dim}, heads={w.M}, "
+                                     f"levels={w.L}, points={w.K}) on the encoder shape "
+                                     f"B={w.B}, Q=S={w.Q}",
+        "dtype": "bf16", "steps": min(args.steps, 200), "warmup": args.warmup,
+        "layer_fwd_bwd_ms": round(layer_ms, 4), "operator_fwd_bwd_ms": round(op_ms, 4),
+        "operator_share": round(op_ms / layer_ms, 3),
+        "layer_queries_per_s": round(w.B * w.Q / (layer_ms * 1e-3), 1),
+        "l2": "flushed before each step (256 MiB write, outside the events)",
+        "accumulator": "fp32_buffer", "data": "synthetic"}), flush=True)
+
+
 def main(argv=None):
     args = parse_args(argv)
+    if args.layer:
+        run_layer(args)
+        return
     if args.sweep:
         run_sweep(args)
     elif args.configs:
