@@ -227,14 +227,20 @@ MSDA_API msda_status_t msda_backward_finish(const void *workspace, size_t worksp
  * - Returns MSDA_ERR_WORKSPACE, before any launch, when a 16-bit problem needs
  *   more than MSDA_STATIC_WORKSPACE_BYTES (B*S*M*D*4 bytes). fp32 data needs no
  *   workspace and has no such limit.
- * - The first call on each device looks up the array's device address with
- *   that device current (MSDA_ERR_CUDA if the lookup fails); make that first
- *   call before any stream capture begins.
+ * - Each call finds the array's device address in the calling thread's
+ *   current context (MSDA_ERR_CUDA if that fails). The address is cached per
+ *   context and looked up again when the context changes (for instance after
+ *   cudaDeviceReset), never reused across contexts. The first call in a
+ *   context may load the library's module; make it before any stream capture
+ *   begins.
  * - Every call shares the one array. Each call clears the part it uses, but
  *   calls that overlap on the GPU (other streams, other host threads) race on
  *   it: the caller must order them.
- * - The array occupies device memory on every GPU where this entry point has
- *   run, until the process exits. */
+ * - The array occupies device memory in every context that has loaded the
+ *   library's module, until the process exits: under the default lazy module
+ *   loading that is the first call of any libmsda entry point that runs a
+ *   kernel on that device; with CUDA_MODULE_LOADING=EAGER it is every device
+ *   the process initialises, as soon as it does. */
 MSDA_API msda_status_t msda_backward_static_workspace(
     const void *value, const int64_t *spatial_shapes, const int64_t *level_start_index,
     const void *sampling_locations, const void *attention_weights,
@@ -262,18 +268,22 @@ MSDA_API msda_status_t msda_debug_corners(const int64_t *spatial_shapes,
  * a memory checker, much slower than libmsda.so. The normal library exports
  * the same three entry points and never sets the word.
  * msda_checked_build: 1 in libmsda_checked.so, 0 in libmsda.so.
- * msda_device_check: synchronizes `stream`, then reads and clears the current
- *   device's fault word: MSDA_ERR_DEVICE_BOUNDS if any checked access was
- *   out of range since the last call, MSDA_OK otherwise (always in the normal
- *   build); MSDA_ERR_CUDA if the synchronization or the readback fails.
+ * msda_device_check: synchronizes `stream`, then reads and clears the fault
+ *   word of the calling thread's current context: MSDA_ERR_DEVICE_BOUNDS if
+ *   any checked access was out of range since the last call, MSDA_OK
+ *   otherwise (always in the normal build); MSDA_ERR_CUDA if the
+ *   synchronization or the readback fails.
  * msda_debug_bounds_self_test: enqueues one range check that must fail (no
  *   memory is accessed), so that the next msda_device_check of the checked
  *   build returns MSDA_ERR_DEVICE_BOUNDS; a no-op check in the normal build.
- * The first call on each device looks up the word's device address; make it
- * before any stream capture begins. */
+ * The word's address is looked up per context and cached with the context's
+ * identity (a new context, e.g. after cudaDeviceReset, gets its own); the
+ * first lookup in a context may load the library's module, so make it before
+ * any stream capture begins. */
 MSDA_API int msda_checked_build(void);
 MSDA_API msda_status_t msda_device_check(void *stream);
 MSDA_API msda_status_t msda_debug_bounds_self_test(void *stream);
+
 
 /* Sample split (launch tuning; process-wide). With one lane group per
  * (b, q, m), a problem with few query-heads -- a detector decoder's B*Q*M =

@@ -52,6 +52,9 @@ msda_status_t check_dims(const msda_dims_t *d, msda_dtype_t dt, int *lpg) {
         d->B > INT32_MAX || d->Q > INT32_MAX)
         return MSDA_ERR_SHAPE;
     if (d->S * d->M * d->D > INT32_MAX) return MSDA_ERR_SHAPE;     // 32-bit row offsets
+    // value-sized tensors (and the fp32 workspace, 4 bytes per element) must
+    // have byte counts that fit in int64: B*S*M*D <= 2^60
+    if (d->B > ((int64_t)1 << 60) / (d->S * d->M * d->D)) return MSDA_ERR_SHAPE;
     const int64_t lk = d->L * d->K;
     if (lk > (1 << 20)) return MSDA_ERR_SHAPE;
     // every element count must fit comfortably in int64

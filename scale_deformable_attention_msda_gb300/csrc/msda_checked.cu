@@ -6,43 +6,21 @@
 // checked build stands in for its memcheck: every global access of every
 // kernel is checked first against the extent of the tensor it belongs to
 // (in_tensor in msda_common.cuh). An access that would leave its tensor is
-// skipped and sets bit 0 of one device word per GPU; the host reads and
+// skipped and sets bit 0 of one device word per context; the host reads and
 // clears that word after a synchronisation. Nothing traps, so a fault found
 // this way leaves the context usable.
 //
-// The word is a file-scope __device__ variable. Host code cannot use its name
-// as a device address, so the first call on each device looks the address up
-// with cudaGetSymbolAddress (that device current) and caches it; make that
-// first call before any stream capture begins.
-#include <mutex>
-
+// The word is a file-scope __device__ variable (msda_runtime.cu). Its device
+// address is looked up in the calling thread's current context and cached
+// with that context's identity, so a new context (after cudaDeviceReset, for
+// instance) gets its own address. The first lookup in a context loads the
+// library's module; make it before any stream capture begins.
 #include "msda_common.cuh"
+#include "msda_host.h"
 
 namespace msda {
 
 namespace {
-
-__device__ unsigned g_fault_word;
-
-constexpr int kMaxDevices = 64;
-std::mutex g_lock;
-unsigned *g_address[kMaxDevices] = {};
-
-cudaError_t fault_word_address(unsigned **out) {
-    int dev = -1;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return e;
-    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-    std::lock_guard<std::mutex> guard(g_lock);
-    if (!g_address[dev]) {
-        void *p = nullptr;
-        e = cudaGetSymbolAddress(&p, g_fault_word);
-        if (e != cudaSuccess) return e;
-        g_address[dev] = static_cast<unsigned *>(p);
-    }
-    *out = g_address[dev];
-    return cudaSuccess;
-}
 
 // One range check that must fail (a NULL tensor of extent 0); no memory access.
 __global__ void bounds_self_test_kernel(const Params p) {
@@ -52,11 +30,11 @@ __global__ void bounds_self_test_kernel(const Params p) {
 
 }  // namespace
 
-// Params::err for a launch: the current device's fault word in the checked
+// Params::err for a launch: the current context's fault word in the checked
 // build, NULL in the normal one.
 cudaError_t fault_word_for_launch(unsigned **err) {
 #ifdef MSDA_CHECKED
-    return fault_word_address(err);
+    return fault_word(err);
 #else
     *err = nullptr;
     return cudaSuccess;
@@ -80,7 +58,7 @@ msda_status_t msda_device_check(void *stream) {
         return MSDA_ERR_CUDA;
 #ifdef MSDA_CHECKED
     unsigned *word = nullptr;
-    if (msda::fault_word_address(&word) != cudaSuccess) return MSDA_ERR_CUDA;
+    if (msda::fault_word(&word) != cudaSuccess) return MSDA_ERR_CUDA;
     unsigned v = 0u;
     if (cudaMemcpy(&v, word, sizeof v, cudaMemcpyDeviceToHost) != cudaSuccess) return MSDA_ERR_CUDA;
     if (v != 0u) {

@@ -11,12 +11,15 @@
 // scratch in a fixed array that belongs to the library.
 //
 // The array is a file-scope __device__ variable of MSDA_STATIC_WORKSPACE_BYTES
-// (declared in msda.h). Every GPU on which this entry point runs holds it
-// until the process exits. Host code cannot use the array's name as a device
-// address (on the host it names a host-side stand-in), so the first call on
-// each device looks up the real address with cudaGetSymbolAddress, with that
-// device current, and caches it; later calls reuse the cached address. That
-// first call should therefore be made before any stream capture begins.
+// (declared in msda.h). Host code cannot use the array's name as a device
+// address (on the host it names a host-side stand-in), so each call looks up
+// the real address with cudaGetSymbolAddress in the calling thread's current
+// context; the address is cached together with that context's identity and
+// looked up again whenever a call comes from another context (for instance
+// the primary context recreated after cudaDeviceReset), so a call never adds
+// through an address of a destroyed context. The first lookup in a context
+// loads the library's module there; make that first call before any stream
+// capture begins.
 //
 // Every call shares the one array and leaves its contents behind. msda_backward
 // zeroes the part a call uses before accumulating into it, so stale contents
@@ -24,34 +27,23 @@
 // streams, or different host threads) race on the array and must be ordered
 // by the caller. Nothing here calls cudaMalloc, cudaFree or any other
 // allocating routine.
-#include <mutex>
+#include <cuda_runtime.h>
 
 #include "msda.h"
-#include <cuda_runtime.h>
+#include "msda_host.h"
 
 namespace {
 
 constexpr size_t kStaticFloats = MSDA_STATIC_WORKSPACE_BYTES / sizeof(float);
-constexpr int kMaxDevices = 64;
 
 __device__ __align__(256) float g_static_workspace[kStaticFloats];
 
-std::mutex g_lock;
-void *g_address[kMaxDevices] = {};
-
-// Device address of g_static_workspace on the current device (looked up once
-// per device, with that device current).
+// Device address of g_static_workspace in the current context.
 msda_status_t static_workspace_address(void **out) {
-    int dev = -1;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return MSDA_ERR_CUDA;
-    std::lock_guard<std::mutex> guard(g_lock);
-    if (!g_address[dev]) {
-        void *p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_static_workspace) != cudaSuccess || !p) return MSDA_ERR_CUDA;
-        g_address[dev] = p;
-    }
-    *out = g_address[dev];
-    return MSDA_OK;
+    return msda::symbol_address(reinterpret_cast<const void *>(&g_static_workspace), out) ==
+                   cudaSuccess
+               ? MSDA_OK
+               : MSDA_ERR_CUDA;
 }
 
 }  // namespace

@@ -74,8 +74,9 @@ def test_traffic_figure_belongs_to_the_instantiation_run():
         assert bench.profiled_traffic(k, "f16", "native") is None
         f32 = bench.profiled_traffic(k, "f32", "fp32_buffer")
         assert f32 is None or f32 != bench.profiled_traffic(k, "bf16", "fp32_buffer")
-    assert bench.profiled_traffic("msda_forward_kernel", "f32", "fp32_buffer") != \
-        bench.profiled_traffic("msda_backward_kernel", "f32", "fp32_buffer")
+    fwd = bench.profiled_traffic("msda_forward_kernel", "f32", "fp32_buffer")
+    bwd = bench.profiled_traffic("msda_backward_kernel", "f32", "fp32_buffer")
+    assert fwd is None or bwd is None or fwd != bwd
     for (k, _, _), name in files.items():
         assert os.path.exists(os.path.join(ROOT, "profiles", name)), name
 

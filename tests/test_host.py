@@ -160,6 +160,24 @@ def test_backward_workspace_rules(so):
     assert _bwd(so, d, grad_value=None) == 1
 
 
+def test_value_sized_byte_counts_cannot_wrap(so):
+    """B*S*M*D is bounded (<= 2^60 elements) so that the fp32 workspace's byte
+    count, B*S*M*D*4, can never wrap around: with S*M*D just under 2^31 and a
+    huge B the dims are refused, and the workspace size is 0 (invalid), not a
+    wrapped small number that would pass the size checks."""
+    smd = 2 ** 31 - 2 ** 13                     # S*M*D < 2^31: allowed on its own
+    d = _dims(S=smd // (8 * 32), M=8, D=32, B=2 ** 31 - 1, Q=1)
+    assert so.msda_backward_workspace_bytes(ctypes.byref(d), 1, 1) == 0
+    assert _bwd(so, d, dtype=1, accum=1) == 2
+    assert _fwd(so, d) == 2
+    static = so.msda_backward_static_workspace
+    vp = ctypes.c_void_p
+    assert static(vp(FAKE), vp(FAKE), vp(FAKE), vp(FAKE), vp(FAKE), vp(None), vp(FAKE), vp(FAKE),
+                  vp(FAKE), vp(FAKE), ctypes.byref(d), 1, vp(0)) != 0
+    ok = _dims(B=2 ** 20, Q=0)                  # large but B*S*M*D < 2^60: still valid
+    assert so.msda_backward_workspace_bytes(ctypes.byref(ok), 1, 1) == 4 * 2 ** 20 * 22223 * 256
+
+
 def test_binding_refuses_cpu_tensors(so):
     from scale_deformable_attention_msda_gb300 import binding
     v = torch.zeros(1, 80, 2, 8)

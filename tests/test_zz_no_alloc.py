@@ -70,6 +70,29 @@ def test_matches_msda_backward_on_two_calls_in_a_row(w, tol):
             assert _rel(g, r) <= tol
 
 
+@pytest.mark.parametrize("dtype,tol", [("bf16", 2e-2), ("f32", 1e-4)])
+def test_matches_the_fp64_oracle_on_the_decoder(dtype, tol):
+    """The allocation-free backward against the fp64 CPU oracle itself (not
+    only against msda_backward), on the decoder shape, two calls in a row."""
+    import oracle
+    oracle.build()
+    w = wl.decoder(dtype)
+    p = wl.make_inputs(w)
+    t = {k: _up(p[k], w.dtype) for k in ("value", "loc", "attn", "grad_out")}
+    t["shapes"] = torch.tensor(p["shapes"]).cuda()
+    t["starts"] = torch.tensor(p["starts"]).cuda()
+    dims = binding.dims_of(t["value"], t["shapes"], t["loc"])
+    ref = oracle.backward(p["value"], p["shapes"], p["starts"], p["loc"], p["attn"],
+                          p["grad_out"])
+    for _ in range(2):
+        got = _static_call(t, dims, w.dtype)
+        torch.cuda.synchronize()
+        for g, r in zip(got, ref):
+            g = g.double().cpu().numpy()
+            assert np.isfinite(g).all()
+            assert np.linalg.norm(g - r) / np.linalg.norm(r) <= tol
+
+
 def test_rejects_a_problem_larger_than_the_static_array():
     # bf16, B*S*M*D*4 bytes = 128 MiB > 64 MiB: refused before any launch
     dims = binding.msda_dims_t(B=4, S=32768, Q=10, M=8, D=32, L=1, K=4)
