@@ -40,8 +40,8 @@ FLUSH_BYTES = 256 << 20
 FALLBACK_HBM_GBS = 6800.0
 # L2 reduction throughput of this machine's GB300 for random 16-byte vector adds,
 # GB/s of reduction data, by bytes each group of lanes adds per instruction
-# (measured by scale_deformable_attention_msda_gb300/probes/memprobe.cu: the
-# 64 MiB footprint rows). The backward is bound by this, not by HBM.
+# (the 64 MiB footprint rows of profiles/gb300_memory_ceilings.md, recorded
+# with a standalone microbenchmark). The backward is bound by this, not by HBM.
 RED_CEILING_GBS = {64: 5902.0, 128: 7003.0}
 
 
@@ -51,7 +51,9 @@ def parse_args(argv=None):
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=100)
     ap.add_argument("--dtype", default="bf16", choices=["bf16", "f32", "f16"])
-    ap.add_argument("--accum", default="fp32_buffer", choices=["fp32_buffer", "native"])
+    ap.add_argument("--accum", default="fp32_buffer", choices=["fp32_buffer", "native", "auto"])
+    ap.add_argument("--no-f32-line", action="store_true",
+                    help="skip the second timed phase with fp32 storage (the line's f32_encoder)")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=50)
@@ -187,7 +189,15 @@ def measured_hbm_peak():
 
 
 ACCUM_MODES = {"fp32_buffer": lambda b: b.MSDA_ACC_FP32_BUFFER,
-               "native": lambda b: b.MSDA_ACC_NATIVE}
+               "native": lambda b: b.MSDA_ACC_NATIVE,
+               "auto": lambda b: b.MSDA_ACC_AUTO}
+
+
+def arithmetic_dtype(storage: str, fp32_target: bool) -> str:
+    """The type the step's arithmetic and grad_value accumulation run in:
+    fp32 for fp32 storage and for 16-bit storage with the fp32 workspace; the
+    16-bit type itself when grad_value is accumulated natively."""
+    return "f32" if (storage == "f32" or fp32_target) else storage
 
 KERNEL_SOURCES = {"msda_forward_kernel": ("msda_common.cuh", "msda_forward.cu"),
                   "msda_backward_kernel": ("msda_common.cuh", "msda_backward.cuh")}
@@ -398,37 +408,93 @@ def run_ours(args):
     barrier(local_rank)
     binding.lib()
 
-    tdt = {"bf16": torch.bfloat16, "f32": torch.float32, "f16": torch.float16}[args.dtype]
     accum = ACCUM_MODES[args.accum](binding)
-    w = wl.encoder(args.dtype, variant=rank)
-    p = wl.make_inputs(w)
-
-    def up(a):
-        return torch.tensor(a, dtype=torch.float64).to(tdt).to(dev)
-
-    value, loc, attn, gout = up(p["value"]), up(p["loc"]), up(p["attn"]), up(p["grad_out"])
-    shapes = torch.tensor(p["shapes"], device=dev)
-    starts = torch.tensor(p["starts"], device=dev)
-    out = torch.empty((w.B, w.Q, w.M * w.D), dtype=tdt, device=dev)
-    buf = binding.BackwardBuffers(value, loc, attn, accum)
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
+    names = ("forward", "zero", "backward", "finish")
 
-    def step(ev=None):
-        if ev:
-            ev[0].record(stream)
-        binding.msda_forward(value, shapes, starts, loc, attn, out=out)
-        if ev:
-            ev[1].record(stream)
-        binding.msda_backward_zero(buf, tdt)
-        if ev:
-            ev[2].record(stream)
-        binding.msda_backward_accumulate(value, shapes, starts, loc, attn, gout, buf)
-        if ev:
-            ev[3].record(stream)
-        binding.msda_backward_finish(buf, tdt)
-        if ev:
-            ev[4].record(stream)
+    def setup(dtype):
+        """Operands of the encoder workload in `dtype`, resident in HBM."""
+        tdt = {"bf16": torch.bfloat16, "f32": torch.float32, "f16": torch.float16}[dtype]
+        w = wl.encoder(dtype, variant=rank)
+        p = wl.make_inputs(w)
+
+        def up(a):
+            return torch.tensor(a, dtype=torch.float64).to(tdt).to(dev)
+
+        return {"w": w, "p": p, "tdt": tdt, "value": up(p["value"]), "loc": up(p["loc"]),
+                "attn": up(p["attn"]), "gout": up(p["grad_out"]),
+                "shapes": torch.tensor(p["shapes"], device=dev),
+                "starts": torch.tensor(p["starts"], device=dev)}
+
+    def timed(op, acc, steps, warmup):
+        """Warm-up, then `steps` timed steps (L2 flushed before each, outside
+        the events); per-kernel event times in ms."""
+        out = torch.empty((op["w"].B, op["w"].Q, op["w"].M * op["w"].D), dtype=op["tdt"], device=dev)
+        buf = binding.BackwardBuffers(op["value"], op["loc"], op["attn"], acc)
+        a = (op["value"], op["shapes"], op["starts"], op["loc"], op["attn"])
+
+        def step(ev=None):
+            if ev:
+                ev[0].record(stream)
+            binding.msda_forward(*a, out=out)
+            if ev:
+                ev[1].record(stream)
+            binding.msda_backward_zero(buf, op["tdt"])
+            if ev:
+                ev[2].record(stream)
+            binding.msda_backward_accumulate(*a, op["gout"], buf)
+            if ev:
+                ev[3].record(stream)
+            binding.msda_backward_finish(buf, op["tdt"])
+            if ev:
+                ev[4].record(stream)
+
+        for _ in range(warmup):
+            flush.fill_(1)
+            step()
+        torch.cuda.synchronize()
+        barrier(local_rank)
+        torch.cuda.synchronize()
+        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(steps)]
+        for i in range(steps):
+            flush.fill_(i & 0xff)
+            step(evs[i])
+        torch.cuda.synchronize()
+        barrier(local_rank)
+        torch.cuda.synchronize()
+        per = {n: [evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(steps)]
+               for j, n in enumerate(names)}
+        step_ms = [evs[i][0].elapsed_time(evs[i][4]) for i in range(steps)]
+        return per, step_ms, buf.workspace_bytes > 0
+
+    peak, peak_kind = measured_hbm_peak()
+    kernel_name = {"forward": "msda_forward_kernel", "backward": "msda_backward_kernel"}
+
+    def roofline_of(w, mean, dtype, acc_name):
+        """Roofline of the dominant kernel from its event times."""
+        cb = wl.compulsory_bytes(w)
+        algo = {"forward": cb["forward"], "backward": cb["backward"]}
+        dominant = max(("forward", "backward"), key=lambda n: mean[n])
+        achieved = algo[dominant] / (mean[dominant] * 1e-3) / 1e9
+        traffic = profiled_traffic(kernel_name[dominant], dtype, acc_name)
+        roof = {"bound": "hbm", "kernel": kernel_name[dominant], "achieved": round(achieved, 1),
+                "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
+                "traffic": traffic, "algorithmic_bytes": algo[dominant],
+                "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
+                else "fallback 6.8 TB/s",
+                "traffic_source": (f"stored ncu figure: profiles/{PROFILE_FILES[(kernel_name[dominant], dtype, acc_name)]}"
+                                   " (dram__bytes_read.sum + dram__bytes_write.sum per launch, "
+                                   "valid while the kernel sources hash as recorded there)")
+                if traffic is not None else "none: no ncu summary of this kernel's current code"}
+        kernels = {}
+        for n in names:
+            k = {"ms": round(mean[n], 5)}
+            if n in algo:
+                gbs = algo[n] / (mean[n] * 1e-3) / 1e9
+                k.update(algorithmic_bytes=algo[n], gbs=round(gbs, 1), hbm_frac=round(gbs / peak, 4))
+            kernels[n] = k
+        return roof, kernels, algo
 
     uuid = None
     try:
@@ -438,28 +504,36 @@ def run_ours(args):
         uuid = None
     sampler = ClockSampler(uuid) if rank == 0 else None
 
-    for _ in range(args.warmup):
-        flush.fill_(1)
-        step()
-    torch.cuda.synchronize()
-    barrier(local_rank)
-    torch.cuda.synchronize()
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
-    for i in range(args.steps):
-        flush.fill_(i & 0xff)
-        step(evs[i])
-    torch.cuda.synchronize()
-    barrier(local_rank)
-    torch.cuda.synchronize()
-    clocks = sampler.stop() if sampler else None
-
-    names = ("forward", "zero", "backward", "finish")
-    per = {n: [evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(args.steps)]
-           for j, n in enumerate(names)}
-    step_ms = [evs[i][0].elapsed_time(evs[i][4]) for i in range(args.steps)]
+    op = setup(args.dtype)
+    w, p = op["w"], op["p"]
+    tdt, value, loc, attn, gout = op["tdt"], op["value"], op["loc"], op["attn"], op["gout"]
+    shapes, starts = op["shapes"], op["starts"]
+    per, step_ms, fp32_target = timed(op, accum, args.steps, args.warmup)
     total_s = sum(step_ms) / 1e3
     qps, slowest_s, total_units = job_throughput(w.B * w.Q * args.steps, total_s, dev)
     ms_per_step = slowest_s * 1e3 / args.steps
+    mean = {n: statistics.fmean(v) for n, v in per.items()}
+    resolved = "fp32_buffer" if fp32_target else "native"
+    acc_name = "fp32_buffer" if args.dtype == "f32" else resolved
+
+    # ---- the same step with fp32 storage (both precisions of the encoder
+    # configuration on one line); fewer steps
+    f32_line = None
+    if args.dtype != "f32" and not args.no_f32_line:
+        op32 = setup("f32")
+        steps32 = max(1, min(args.steps, 500))
+        per32, step32, _ = timed(op32, binding.MSDA_ACC_FP32_BUFFER, steps32, args.warmup)
+        qps32, slow32, _ = job_throughput(op32["w"].B * op32["w"].Q * steps32, sum(step32) / 1e3, dev)
+        mean32 = {n: statistics.fmean(v) for n, v in per32.items()}
+        roof32, kern32, _ = roofline_of(op32["w"], mean32, "f32", "fp32_buffer")
+        f32_line = {"storage_dtype": "f32", "dtype": "f32", "grad_value_accumulator": "fp32 atomics",
+                    "value": round(qps32, 1), "unit": UNIT, "steps": steps32,
+                    "ms_per_step": round(slow32 * 1e3 / steps32, 5), "kernels": kern32,
+                    "roofline": roof32, "gpu_launches": 3 * steps32,
+                    "step": "msda_forward + msda_backward (zero, accumulate; fp32 data needs no "
+                            "finish pass)"}
+        del op32
+    clocks = sampler.stop() if sampler else None
 
     # ---- end to end through the public API, host buffers, copies timed.
     # Pipelined as a training input pipeline runs: step i's inputs go in on
@@ -474,26 +548,10 @@ def run_ours(args):
         e2e = run_e2e(args, binding, torch, p, w, tdt, accum, shapes, starts, stream, dev)
 
     # ---- roofline of the dominant kernel
-    cb = wl.compulsory_bytes(w)
-    algo = {"forward": cb["forward"], "backward": cb["backward"]}
-    mean = {n: statistics.fmean(v) for n, v in per.items()}
-    dominant = max(("forward", "backward"), key=lambda n: mean[n])
-    peak, peak_kind = measured_hbm_peak()
-    kernel_name = {"forward": "msda_forward_kernel", "backward": "msda_backward_kernel"}
-    achieved = algo[dominant] / (mean[dominant] * 1e-3) / 1e9
-    traffic = profiled_traffic(kernel_name[dominant], args.dtype, args.accum)
-    roofline = {"bound": "hbm", "kernel": kernel_name[dominant], "achieved": round(achieved, 1),
-                "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
-                "traffic": traffic, "algorithmic_bytes": algo[dominant],
-                "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
-                else "fallback 6.8 TB/s"}
-    kernels = {}
+    roofline, kernels, _ = roofline_of(w, mean, args.dtype, acc_name)
     for n in names:
-        k = {"ms": round(mean[n], 5), "launches": args.steps}
-        if n in algo:
-            gbs = algo[n] / (mean[n] * 1e-3) / 1e9
-            k.update(algorithmic_bytes=algo[n], gbs=round(gbs, 1), hbm_frac=round(gbs / peak, 4))
-        kernels[n] = k
+        kernels[n]["launches"] = args.steps
+    cb = wl.compulsory_bytes(w)
     step_bytes = cb["forward"] + cb["backward"]
     # Atomic bytes the backward adds per launch (the distinct corner rows it
     # issues, at the target's element size) and the bytes one add instruction
@@ -501,7 +559,7 @@ def run_ours(args):
     # workspace use D/4 lanes of 4 fp32 channels while D/4 fits a warp (4 D
     # bytes per query-head; 16-byte lanes with 16-bit data write 2 D, in two
     # halves); native 16-bit mode uses D/8 lanes of 8 channels (2 D bytes).
-    f32_target = args.dtype == "f32" or accum == binding.MSDA_ACC_FP32_BUFFER
+    f32_target = args.dtype == "f32" or fp32_target
     narrow = f32_target and w.D // 4 <= 32
     lanes = w.D // 4 if narrow else w.D // 8
     acc_bytes = 4 if f32_target else 2
@@ -516,7 +574,7 @@ def run_ours(args):
                        "atomic_bytes_unmerged": w.samples * 4 * w.D * acc_bytes,
                        "atomic_bytes_per_level": [n * w.D * acc_bytes for n in rows_per_level],
                        "peak_source": "measured red.global.add.v4 throughput, "
-                                      f"{group}-byte groups (probes/memprobe.cu)"}
+                                      f"{group}-byte groups (profiles/gb300_memory_ceilings.md)"}
 
     result = None
     if rank == 0:
@@ -524,15 +582,16 @@ def run_ours(args):
         if world == 1 and not args.no_cpu_baseline:
             cpu = cpu_baseline(p)
         # forward, zero (grad_value and/or workspace), accumulate, finish
-        launches_per_step = 4 if (args.dtype != "f32" and accum == binding.MSDA_ACC_FP32_BUFFER) else 3
+        launches_per_step = 4 if (args.dtype != "f32" and fp32_target) else 3
         result = {
             "metric": METRIC, "value": round(qps, 1), "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-            "dtype": "f32", "data": "synthetic",
+            "dtype": arithmetic_dtype(args.dtype, fp32_target), "data": "synthetic",
             "config": {"workload": "deformable-detr encoder: B=2, Q=S=22223, M=8, D=32, L=4, K=4, "
                                    "levels (100,167),(50,84),(25,42),(13,21)",
                        "storage_dtype": args.dtype, "grad_value_accumulator": args.accum,
+                       "accumulator_resolved": acc_name,
                        "global_batch": w.B * world, "queries_per_step": w.B * w.Q * world,
                        "parallelism": f"replicas x{world}" if world > 1 else "single gpu",
                        "l2": "flushed between timed steps (256 MiB write, outside the events)",
@@ -542,6 +601,7 @@ def run_ours(args):
                          "frac": round(step_bytes / (ms_per_step * 1e-3) / 1e9 / peak, 4)},
             "kernels": kernels,
             "roofline": roofline,
+            "f32_encoder": f32_line,
             "atomic_roofline": atomic_roofline,
             "cpu_baseline": cpu,
             "e2e": e2e,

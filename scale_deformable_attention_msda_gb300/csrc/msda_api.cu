@@ -30,6 +30,17 @@ bool dtype_ok(msda_dtype_t dt) {
 }
 bool is_16bit(msda_dtype_t dt) { return dt == MSDA_BF16 || dt == MSDA_F16; }
 int elem_bytes(msda_dtype_t dt) { return dt == MSDA_F64 ? 8 : (dt == MSDA_F32 ? 4 : 2); }
+
+// MSDA_ACC_AUTO, resolved on the host from the sizes alone: native
+// accumulation when the value rows receive on average at most kAutoMeanAdds
+// corner adds per head (4 Q K L <= kAutoMeanAdds S), the fp32 workspace
+// otherwise. Other modes are returned unchanged.
+constexpr int64_t kAutoMeanAdds = 4;
+msda_accum_t resolve_accum(const msda_dims_t &d, msda_accum_t accum) {
+    if (accum != MSDA_ACC_AUTO) return accum;
+    const double adds = 4.0 * (double)d.Q * (double)d.K * (double)d.L;
+    return adds <= (double)kAutoMeanAdds * (double)d.S ? MSDA_ACC_NATIVE : MSDA_ACC_FP32_BUFFER;
+}
 bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
 // Lanes per (b,q,m) group: D / (channels per 16 bytes), a power of two <= 32.
@@ -188,7 +199,7 @@ msda_status_t msda_forward_softmax(const void *value, const int64_t *spatial_sha
 size_t msda_backward_workspace_bytes(const msda_dims_t *dims, msda_dtype_t dtype,
                                      msda_accum_t accum) {
     if (check_dims(dims, dtype, nullptr) != MSDA_OK) return 0;
-    if (!is_16bit(dtype) || accum != MSDA_ACC_FP32_BUFFER) return 0;
+    if (!is_16bit(dtype) || resolve_accum(*dims, accum) != MSDA_ACC_FP32_BUFFER) return 0;
     return (size_t)(dims->B * dims->S * dims->M * dims->D) * sizeof(float);
 }
 
@@ -208,8 +219,10 @@ msda_status_t plan_target(void *grad_value, void *workspace, size_t workspace_by
                           BackwardPlan *bp) {
     msda_status_t st = check_dims(dims, dtype, &bp->lpg);
     if (st != MSDA_OK) return st;
-    if (accum != MSDA_ACC_NATIVE && accum != MSDA_ACC_FP32_BUFFER) return MSDA_ERR_DTYPE;
+    if (accum != MSDA_ACC_NATIVE && accum != MSDA_ACC_FP32_BUFFER && accum != MSDA_ACC_AUTO)
+        return MSDA_ERR_DTYPE;
     const msda_dims_t &d = *dims;
+    accum = resolve_accum(d, accum);
     bp->f32acc = is_16bit(dtype) && accum == MSDA_ACC_FP32_BUFFER;
     bp->nval = d.B * d.S * d.M * d.D;
     bp->target = bp->f32acc ? workspace : grad_value;

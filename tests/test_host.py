@@ -178,6 +178,29 @@ def test_value_sized_byte_counts_cannot_wrap(so):
     assert so.msda_backward_workspace_bytes(ctypes.byref(ok), 1, 1) == 4 * 2 ** 20 * 22223 * 256
 
 
+def test_auto_accumulation_is_resolved_from_the_sizes(so):
+    """MSDA_ACC_AUTO is native when 4 Q K L <= 4 S (at most 4 corner adds per
+    value row and head on average) and the fp32 buffer otherwise; the
+    workspace size and every backward call agree (no CUDA call here)."""
+    vp = ctypes.c_void_p
+    dec = _dims(Q=300)                                  # 0.9 adds per row: native
+    enc = _dims(Q=22223)                                # 64 adds per row: fp32 buffer
+    n = 2 * 22223 * 8 * 32
+    assert so.msda_backward_workspace_bytes(ctypes.byref(dec), 1, 2) == 0
+    assert so.msda_backward_workspace_bytes(ctypes.byref(enc), 1, 2) == 4 * n
+    assert so.msda_backward_workspace_bytes(ctypes.byref(enc), 0, 2) == 0          # fp32 data
+    edge = _dims(Q=22223, K=1, L=1)                     # exactly 4 adds per row: native
+    assert so.msda_backward_workspace_bytes(ctypes.byref(edge), 1, 2) == 0
+    over = _dims(Q=22224, K=1, L=1)
+    assert so.msda_backward_workspace_bytes(ctypes.byref(over), 1, 2) == 4 * n
+    assert _bwd(so, enc, dtype=1, accum=2, ws=None) == 5          # the fp32 buffer needs one
+    assert _bwd(so, dec, dtype=1, accum=2, grad_value=None) == 1  # native: no workspace asked
+    assert so.msda_backward_zero(vp(FAKE), vp(None), ctypes.c_size_t(0), 2, ctypes.byref(enc),
+                                 1, vp(0)) == 5
+    assert _bwd(so, enc, dtype=1, accum=3) == 3                   # unknown mode
+    assert _bwd(so, _dims(B=0), dtype=1, accum=2) == 0            # empty: nothing launched
+
+
 def test_binding_refuses_cpu_tensors(so):
     from scale_deformable_attention_msda_gb300 import binding
     v = torch.zeros(1, 80, 2, 8)
