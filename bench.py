@@ -697,9 +697,10 @@ def run_configs(args):
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
     peak = measured_hbm_peak()[0]
     plan = [(wl.decoder, "f32", "fp32_buffer"), (wl.decoder, "bf16", "fp32_buffer"),
+            (wl.decoder, "bf16", "native"), (wl.decoder, "bf16", "auto"),
             (wl.encoder, "f32", "fp32_buffer"), (wl.encoder, "bf16", "fp32_buffer"),
-            (wl.encoder, "bf16", "native"), (wl.mask2former, "bf16", "fp32_buffer"),
-            (wl.mask2former, "bf16", "native"),
+            (wl.encoder, "bf16", "native"), (wl.encoder, "bf16", "auto"),
+            (wl.mask2former, "bf16", "fp32_buffer"), (wl.mask2former, "bf16", "native"),
             (lambda dt: wl.sweep(5000, 4, 4, dtype=dt), "bf16", "fp32_buffer")]
     for make, dtype, acc_name in plan:
         w = make(dtype)
@@ -763,6 +764,8 @@ def run_configs(args):
         q = w.B * w.Q
         print(json.dumps({
             "config": w.name, "dtype": dtype, "accum": acc_name if dtype != "f32" else "fp32",
+            "accum_resolved": ("fp32_buffer" if buf.workspace_bytes > 0 else "native")
+                              if dtype != "f32" else "fp32",
             "B": w.B, "Q": w.Q, "S": w.S, "samples": w.samples, **t,
             "queries_per_s_cold": round(q / ((t["forward_cold_us"] + t["backward_cold_us"]) * 1e-6), 1),
             "forward_hbm_frac_cold": round(cb["forward"] / (t["forward_cold_us"] * 1e-6) / 1e9 / peak, 4),

@@ -73,6 +73,13 @@ typedef enum {
 /* How msda_backward accumulates grad_value for a 16-bit dtype.
  * NATIVE: vector atomic adds straight into the 16-bit grad_value (each add
  *   rounds to the 16-bit format, so the result depends on contention).
+ *   Measured grad_value error against an fp64 reference (relative L2, bf16,
+ *   GB300): decoder shape 3.3e-3, Mask2Former encoder 1.2e-2, Deformable-DETR
+ *   encoder 1.9e-2 (at the 2e-2 bar: a level-3 pixel receives about 1,300
+ *   adds per head), and 5.5e-2 when every point of 5,000 queries falls in one
+ *   4x4 patch per level: NATIVE misses 2e-2 on contended maps. fp16 keeps 3
+ *   more mantissa bits (decoder 4.1e-4). FP32_BUFFER stays at the 16-bit
+ *   rounding of the result (1.7e-3 bf16) on every one of them.
  * FP32_BUFFER: atomic adds into a caller-provided fp32 workspace, then one
  *   rounding pass into grad_value. For MSDA_F32 and MSDA_F64 both modes are
  *   the same (atomics of that type into grad_value) and no workspace is needed.
@@ -268,7 +275,12 @@ MSDA_API msda_status_t msda_backward_static_workspace(
  * (b,q,m,l,k)) and corner c in order 00, 01, 10, 11, writes to the device
  * array corner_rows (B*Q*M*L*K*4 int32) the value row
  * level_start_index[l] + yy*W_l + xx of a corner inside the map, -1 for a
- * corner outside it. D of dims is not used. */
+ * corner outside it -- the row the loop of the msda-triton course, ch. 1
+ * "The simplest possible implementation", reads for that corner after its
+ * bounds test. One int32 per corner carries both the corner index and its
+ * in-map mask (-1), in place of a separate (x0, y0) pair and 4-bit mask.
+ * D of dims is not used. Errors: MSDA_ERR_NULL, _SHAPE, _DTYPE, _ALIGN before
+ * any launch (corner_rows 16-byte aligned); MSDA_ERR_CUDA on a rejected launch. */
 MSDA_API msda_status_t msda_debug_corners(const int64_t *spatial_shapes,
                                  const int64_t *level_start_index,
                                  const void *sampling_locations,
@@ -313,10 +325,11 @@ MSDA_API msda_status_t msda_debug_bounds_self_test(void *stream);
  * leaves the setting unchanged. */
 MSDA_API msda_status_t msda_set_sample_split(int log2_groups);
 
-/* Static description of a status code (never NULL). */
+/* Static description of a status code (never NULL). Host only; the pages
+ * define no such call: it names the statuses above for error messages. */
 MSDA_API const char *msda_status_string(msda_status_t status);
 
-/* Library version, major*10000 + minor*100 + patch. */
+/* Library version, major*10000 + minor*100 + patch. Host only. */
 MSDA_API int msda_version(void);
 
 #ifdef __cplusplus

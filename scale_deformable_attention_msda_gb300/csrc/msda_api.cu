@@ -125,7 +125,7 @@ msda_status_t check_common(const void *value, const int64_t *shapes, const int64
 
 extern "C" {
 
-int msda_version(void) { return 100; }
+int msda_version(void) { return 200; }
 
 msda_status_t msda_set_sample_split(int log2_groups) {
     if (log2_groups < -1 || log2_groups > 3) return MSDA_ERR_SHAPE;

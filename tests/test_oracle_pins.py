@@ -341,12 +341,30 @@ def test_golden_level_tables():
         assert wl.level_start_index(levels).tolist() == expect
 
 
-def test_golden_counts():
+def test_golden_counts(oracle_mod):
+    """The pages' counts, reached through the oracle: on the decoder shape
+    with every sample strictly inside its map, oracle.corners must give each
+    query M*L*K samples of 4 in-map corners each, and those corners times D
+    channels must land in the pages' "roughly twenty million" multiply-adds."""
     rows = dict(_read_golden("counts.txt"))
-    assert int(rows["reads_per_query M=8 L=4 K=4"]) == 8 * 4 * 4
+    reads = int(rows["reads_per_query M=8 L=4 K=4"])
     lo, hi = (int(v) for v in rows["multiply_adds B=4 Q=300 M=8 D=32 L=4 K=4"].split())
-    w = wl.Workload("c", B=4, Q=300, M=8, D=32, K=4, levels=wl.LEVELS_DETR)
-    assert lo <= wl.multiply_adds(w) <= hi
+    B, Q, M, D, L, K = 4, 300, 8, 32, 4, 4
+    shapes = wl.spatial_shapes(wl.LEVELS_DETR)
+    starts = wl.level_start_index(wl.LEVELS_DETR)
+    rng = np.random.Generator(np.random.PCG64(11))
+    hw = shapes.astype(np.float64)                       # (L, 2) = (H, W)
+    # pixel coordinates in [0.1, dim - 1.1]: all four corners inside the map
+    px = 0.1 + rng.random((B, Q, M, L, K)) * (hw[:, 1][None, None, None, :, None] - 1.2)
+    py = 0.1 + rng.random((B, Q, M, L, K)) * (hw[:, 0][None, None, None, :, None] - 1.2)
+    loc = np.stack([(px + 0.5) / hw[:, 1][None, None, None, :, None],
+                    (py + 0.5) / hw[:, 0][None, None, None, :, None]], axis=-1)
+    c = oracle_mod.corners(shapes, starts, loc)          # (B, Q, M, L, K, 4) rows, -1 off the map
+    assert c.shape == (B, Q, M, L, K, 4)
+    in_map = c >= 0
+    samples_per_query = np.count_nonzero(in_map.any(axis=-1).reshape(B, Q, -1), axis=-1)
+    assert (samples_per_query == reads).all()
+    assert lo <= int(np.count_nonzero(in_map)) * D <= hi
 
 
 def test_workload_shapes_and_seeds():
