@@ -45,6 +45,7 @@ def test_self_test_sets_and_clears_the_fault_word():
 
 @pytest.mark.parametrize("w,accum", [(wl.tiny(), FP32BUF), (wl.decoder("bf16"), FP32BUF),
                                      (wl.decoder("bf16"), NATIVE), (wl.decoder("f16"), FP32BUF),
+                                     (wl.decoder("bf16"), binding.MSDA_ACC_AUTO),
                                      (wl.decoder("f64"), FP32BUF), (wl.sweep(5000, 4, 4), FP32BUF),
                                      (wl.encoder("bf16"), FP32BUF)],
                          ids=lambda x: getattr(x, "name", str(x)))

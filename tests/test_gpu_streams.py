@@ -36,7 +36,8 @@ def _run(t, stream=None, buf=None):
     kw = {}
     if buf is not None:
         kw = dict(grad_value=buf.grad_value, grad_sampling_locations=buf.grad_sampling_locations,
-                  grad_attention_weights=buf.grad_attention_weights, workspace=buf.workspace)
+                  grad_attention_weights=buf.grad_attention_weights, workspace=buf.workspace,
+                  accum=buf.accum)
     gv, gl, ga = binding.msda_backward(t["value"], t["shapes"], t["starts"], t["loc"], t["attn"],
                                        t["grad_out"], stream=stream, **kw)
     return out, gv, gl, ga
@@ -102,3 +103,29 @@ def test_cuda_graph_capture_and_replay():
     fresh = _run(t2)
     torch.cuda.synchronize()
     assert torch.equal(outs[0], fresh[0]) and torch.equal(outs[2], fresh[2])
+
+
+def test_cuda_graph_with_auto_accumulation():
+    """MSDA_ACC_AUTO is resolved on the host, so a captured call replays the
+    mode it resolved to: on the decoder shape native adds with no workspace,
+    zeroing grad_value on every replay."""
+    t = _inputs(wl.decoder("bf16"))
+    buf = binding.BackwardBuffers(t["value"], t["loc"], t["attn"], binding.MSDA_ACC_AUTO)
+    assert buf.workspace is None                    # resolved to native: nothing to allocate
+    eager = [x.clone() for x in _run(t, buf=buf)]
+    torch.cuda.synchronize()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        _run(t, stream=s, buf=buf)
+    torch.cuda.current_stream().wait_stream(s)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        outs = _run(t, stream=torch.cuda.current_stream(), buf=buf)
+    for _ in range(3):
+        buf.grad_value.fill_(7.0)
+        g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(outs[0], eager[0]) and torch.equal(outs[2], eager[2])
+    assert torch.equal(outs[3], eager[3])
+    assert _close(outs[1], eager[1])
