@@ -15,7 +15,7 @@ timed region), the fp64 CPU oracle timed on the host cores as a baseline, and
 the SM clocks sampled during the run.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--dtype bf16|f32|f16]
-                  [--accum fp32_buffer|native] [--impl ours|reference]
+                  [--accum fp32_buffer|native|auto|fp16_buffer] [--impl ours|reference]
 Under torchrun each rank runs its own replica (weak scaling); the time is the
 maximum over ranks. --impl reference times the fp64 CPU oracle instead.
 """
@@ -51,7 +51,7 @@ def parse_args(argv=None):
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=100)
     ap.add_argument("--dtype", default="bf16", choices=["bf16", "f32", "f16"])
-    ap.add_argument("--accum", default="fp32_buffer", choices=["fp32_buffer", "native", "auto"])
+    ap.add_argument("--accum", default="fp32_buffer", choices=["fp32_buffer", "native", "auto", "fp16_buffer"])
     ap.add_argument("--no-f32-line", action="store_true",
                     help="skip the second timed phase with fp32 storage (the line's f32_encoder)")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
@@ -190,14 +190,30 @@ def measured_hbm_peak():
 
 ACCUM_MODES = {"fp32_buffer": lambda b: b.MSDA_ACC_FP32_BUFFER,
                "native": lambda b: b.MSDA_ACC_NATIVE,
-               "auto": lambda b: b.MSDA_ACC_AUTO}
+               "auto": lambda b: b.MSDA_ACC_AUTO,
+               "fp16_buffer": lambda b: b.MSDA_ACC_FP16_BUFFER}
 
 
-def arithmetic_dtype(storage: str, fp32_target: bool) -> str:
+def arithmetic_dtype(storage: str, resolved: str) -> str:
     """The type the step's arithmetic and grad_value accumulation run in:
-    fp32 for fp32 storage and for 16-bit storage with the fp32 workspace; the
-    16-bit type itself when grad_value is accumulated natively."""
-    return "f32" if (storage == "f32" or fp32_target) else storage
+    fp32 for fp32 storage and for 16-bit storage with the fp32 workspace; fp16
+    for bf16 storage with the scaled fp16 workspace; the 16-bit type itself
+    when grad_value is accumulated natively."""
+    if storage == "f32" or resolved == "fp32_buffer":
+        return "f32"
+    return "f16" if resolved == "fp16_buffer" else storage
+
+
+def resolved_accumulator(storage: str, mode: str, workspace_bytes: int) -> str:
+    """What a backward call of `mode` accumulates grad_value in: fp32 storage
+    adds fp32; the scaled fp16 workspace applies to bf16 data only (others add
+    natively); AUTO and the fp32 buffer resolve to the workspace when the
+    library asks for one."""
+    if storage == "f32":
+        return "fp32_buffer"
+    if mode == "fp16_buffer":
+        return "fp16_buffer" if storage == "bf16" else "native"
+    return "fp32_buffer" if workspace_bytes > 0 else "native"
 
 KERNEL_SOURCES = {"msda_forward_kernel": ("msda_common.cuh", "msda_forward.cu"),
                   "msda_backward_kernel": ("msda_common.cuh", "msda_backward.cuh")}
@@ -427,12 +443,18 @@ def run_ours(args):
                 "shapes": torch.tensor(p["shapes"], device=dev),
                 "starts": torch.tensor(p["starts"], device=dev)}
 
-    def timed(op, acc, steps, warmup):
+    def timed(op, acc, acc_name, steps, warmup):
         """Warm-up, then `steps` timed steps (L2 flushed before each, outside
-        the events); per-kernel event times in ms."""
+        the events); per-kernel event times in ms, and the accumulator the
+        backward resolved to. The scaled fp16 workspace is taken only by the
+        one-call msda_backward: its "backward" time then covers its prepare
+        pass, the adds and its finish pass, and "zero" and "finish" are empty."""
         out = torch.empty((op["w"].B, op["w"].Q, op["w"].M * op["w"].D), dtype=op["tdt"], device=dev)
         buf = binding.BackwardBuffers(op["value"], op["loc"], op["attn"], acc)
         a = (op["value"], op["shapes"], op["starts"], op["loc"], op["attn"])
+        storage = {torch.bfloat16: "bf16", torch.float16: "f16", torch.float32: "f32"}[op["tdt"]]
+        resolved = resolved_accumulator(storage, acc_name, buf.workspace_bytes)
+        one_call = resolved == "fp16_buffer"
 
         def step(ev=None):
             if ev:
@@ -440,13 +462,21 @@ def run_ours(args):
             binding.msda_forward(*a, out=out)
             if ev:
                 ev[1].record(stream)
-            binding.msda_backward_zero(buf, op["tdt"])
+            if not one_call:
+                binding.msda_backward_zero(buf, op["tdt"])
             if ev:
                 ev[2].record(stream)
-            binding.msda_backward_accumulate(*a, op["gout"], buf)
+            if one_call:
+                binding.msda_backward(*a, op["gout"], accum=acc, grad_value=buf.grad_value,
+                                      grad_sampling_locations=buf.grad_sampling_locations,
+                                      grad_attention_weights=buf.grad_attention_weights,
+                                      workspace=buf.workspace)
+            else:
+                binding.msda_backward_accumulate(*a, op["gout"], buf)
             if ev:
                 ev[3].record(stream)
-            binding.msda_backward_finish(buf, op["tdt"])
+            if not one_call:
+                binding.msda_backward_finish(buf, op["tdt"])
             if ev:
                 ev[4].record(stream)
 
@@ -466,7 +496,7 @@ def run_ours(args):
         per = {n: [evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(steps)]
                for j, n in enumerate(names)}
         step_ms = [evs[i][0].elapsed_time(evs[i][4]) for i in range(steps)]
-        return per, step_ms, buf.workspace_bytes > 0
+        return per, step_ms, resolved
 
     peak, peak_kind = measured_hbm_peak()
     kernel_name = {"forward": "msda_forward_kernel", "backward": "msda_backward_kernel"}
@@ -487,6 +517,9 @@ def run_ours(args):
                                    " (dram__bytes_read.sum + dram__bytes_write.sum per launch, "
                                    "valid while the kernel sources hash as recorded there)")
                 if traffic is not None else "none: no ncu summary of this kernel's current code"}
+        if acc_name == "fp16_buffer" and dominant == "backward":
+            roof["duration_covers"] = ("the one msda_backward call: zero + maxima, scale, the "
+                                       "kernel, finish")
         kernels = {}
         for n in names:
             k = {"ms": round(mean[n], 5)}
@@ -508,13 +541,11 @@ def run_ours(args):
     w, p = op["w"], op["p"]
     tdt, value, loc, attn, gout = op["tdt"], op["value"], op["loc"], op["attn"], op["gout"]
     shapes, starts = op["shapes"], op["starts"]
-    per, step_ms, fp32_target = timed(op, accum, args.steps, args.warmup)
+    per, step_ms, acc_name = timed(op, accum, args.accum, args.steps, args.warmup)
     total_s = sum(step_ms) / 1e3
     qps, slowest_s, total_units = job_throughput(w.B * w.Q * args.steps, total_s, dev)
     ms_per_step = slowest_s * 1e3 / args.steps
     mean = {n: statistics.fmean(v) for n, v in per.items()}
-    resolved = "fp32_buffer" if fp32_target else "native"
-    acc_name = "fp32_buffer" if args.dtype == "f32" else resolved
 
     # ---- the same step with fp32 storage (both precisions of the encoder
     # configuration on one line); fewer steps
@@ -522,7 +553,8 @@ def run_ours(args):
     if args.dtype != "f32" and not args.no_f32_line:
         op32 = setup("f32")
         steps32 = max(1, min(args.steps, 500))
-        per32, step32, _ = timed(op32, binding.MSDA_ACC_FP32_BUFFER, steps32, args.warmup)
+        per32, step32, _ = timed(op32, binding.MSDA_ACC_FP32_BUFFER, "fp32_buffer", steps32,
+                                 args.warmup)
         qps32, slow32, _ = job_throughput(op32["w"].B * op32["w"].Q * steps32, sum(step32) / 1e3, dev)
         mean32 = {n: statistics.fmean(v) for n, v in per32.items()}
         roof32, kern32, _ = roofline_of(op32["w"], mean32, "f32", "fp32_buffer")
@@ -558,8 +590,9 @@ def run_ours(args):
     # covers per query-head. fp32 data and 16-bit data with the fp32
     # workspace use D/4 lanes of 4 fp32 channels while D/4 fits a warp (4 D
     # bytes per query-head; 16-byte lanes with 16-bit data write 2 D, in two
-    # halves); native 16-bit mode uses D/8 lanes of 8 channels (2 D bytes).
-    f32_target = args.dtype == "f32" or fp32_target
+    # halves); native 16-bit mode and the fp16 workspace use D/8 lanes of 8
+    # channels (2 D bytes).
+    f32_target = acc_name == "fp32_buffer"
     narrow = f32_target and w.D // 4 <= 32
     lanes = w.D // 4 if narrow else w.D // 8
     acc_bytes = 4 if f32_target else 2
@@ -575,19 +608,23 @@ def run_ours(args):
                        "atomic_bytes_per_level": [n * w.D * acc_bytes for n in rows_per_level],
                        "peak_source": "measured red.global.add.v4 throughput, "
                                       f"{group}-byte groups (profiles/gb300_memory_ceilings.md)"}
+    if acc_name == "fp16_buffer":
+        atomic_roofline["duration_covers"] = "the one msda_backward call (prepare and finish passes too)"
 
     result = None
     if rank == 0:
         cpu = None
         if world == 1 and not args.no_cpu_baseline:
             cpu = cpu_baseline(p)
-        # forward, zero (grad_value and/or workspace), accumulate, finish
-        launches_per_step = 4 if (args.dtype != "f32" and fp32_target) else 3
+        # forward, zero (grad_value and/or workspace), accumulate, finish; the
+        # fp16 workspace: forward, zero + maxima, scale, accumulate, finish
+        launches_per_step = {"fp16_buffer": 5}.get(
+            acc_name, 4 if (args.dtype != "f32" and acc_name == "fp32_buffer") else 3)
         result = {
             "metric": METRIC, "value": round(qps, 1), "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-            "dtype": arithmetic_dtype(args.dtype, fp32_target), "data": "synthetic",
+            "dtype": arithmetic_dtype(args.dtype, acc_name), "data": "synthetic",
             "config": {"workload": "deformable-detr encoder: B=2, Q=S=22223, M=8, D=32, L=4, K=4, "
                                    "levels (100,167),(50,84),(25,42),(13,21)",
                        "storage_dtype": args.dtype, "grad_value_accumulator": args.accum,
@@ -595,7 +632,10 @@ def run_ours(args):
                        "global_batch": w.B * world, "queries_per_step": w.B * w.Q * world,
                        "parallelism": f"replicas x{world}" if world > 1 else "single gpu",
                        "l2": "flushed between timed steps (256 MiB write, outside the events)",
-                       "step": "msda_forward + msda_backward (zero, accumulate, finish)"},
+                       "step": "msda_forward + msda_backward (zero, accumulate, finish)"
+                               if acc_name != "fp16_buffer" else
+                               "msda_forward + msda_backward (one call: zero + maxima, scale, "
+                               "accumulate, finish)"},
             "step_hbm": {"compulsory_bytes": step_bytes,
                          "gbs": round(step_bytes / (ms_per_step * 1e-3) / 1e9, 1),
                          "frac": round(step_bytes / (ms_per_step * 1e-3) / 1e9 / peak, 4)},
@@ -700,7 +740,9 @@ def run_configs(args):
             (wl.decoder, "bf16", "native"), (wl.decoder, "bf16", "auto"),
             (wl.encoder, "f32", "fp32_buffer"), (wl.encoder, "bf16", "fp32_buffer"),
             (wl.encoder, "bf16", "native"), (wl.encoder, "bf16", "auto"),
+            (wl.decoder, "bf16", "fp16_buffer"), (wl.encoder, "bf16", "fp16_buffer"),
             (wl.mask2former, "bf16", "fp32_buffer"), (wl.mask2former, "bf16", "native"),
+            (wl.mask2former, "bf16", "fp16_buffer"),
             (lambda dt: wl.sweep(5000, 4, 4, dtype=dt), "bf16", "fp32_buffer")]
     for make, dtype, acc_name in plan:
         w = make(dtype)
@@ -764,7 +806,7 @@ def run_configs(args):
         q = w.B * w.Q
         print(json.dumps({
             "config": w.name, "dtype": dtype, "accum": acc_name if dtype != "f32" else "fp32",
-            "accum_resolved": ("fp32_buffer" if buf.workspace_bytes > 0 else "native")
+            "accum_resolved": resolved_accumulator(dtype, acc_name, buf.workspace_bytes)
                               if dtype != "f32" else "fp32",
             "B": w.B, "Q": w.Q, "S": w.S, "samples": w.samples, **t,
             "queries_per_s_cold": round(q / ((t["forward_cold_us"] + t["backward_cold_us"]) * 1e-6), 1),

@@ -89,8 +89,24 @@ typedef enum {
 typedef enum {
     MSDA_ACC_NATIVE = 0,
     MSDA_ACC_FP32_BUFFER = 1,
-    MSDA_ACC_AUTO = 2
+    MSDA_ACC_AUTO = 2,
+    MSDA_ACC_FP16_BUFFER = 3
 } msda_accum_t;
+/* MSDA_ACC_FP16_BUFFER (bf16 data; msda_backward and msda_backward_softmax
+ * only -- the three-step calls below refuse it with MSDA_ERR_DTYPE, since its
+ * zero step reads grad_out): native 16-bit atomic adds, but into an fp16
+ * workspace, which keeps 11 significant bits where bf16 keeps 8, with every
+ * contribution multiplied by a power of two 2^k chosen per call; grad_value is
+ * then round(ws * 2^-k). Each element of grad_value sums |a| w |g| over the
+ * samples that reach it (bilinear weight w <= 1, one sample per query, level
+ * and point at most), so no sum exceeds max|grad_out| * Q * A, with A = 1 for
+ * msda_backward_softmax (probabilities) and L * K * max|attention weight|
+ * otherwise; 2^k puts that bound in [2^14, 2^15), below fp16's largest finite
+ * value, whatever the inputs. Sums below 2^-29 of the bound fall into fp16's
+ * subnormals and keep fewer bits. The adds move 64 bytes per corner and head,
+ * as native accumulation does (half the fp32 buffer's).
+ * Workspace: B*S*M*D*2 + 20480 bytes (msda_backward_workspace_bytes). For
+ * fp16, fp32 and fp64 data it is the same as MSDA_ACC_NATIVE. */
 /* MSDA_ACC_AUTO (16-bit data): NATIVE or FP32_BUFFER, chosen on the host from
  * the sizes alone. The call adds natively when the value rows receive on
  * average at most 4 corner adds per head, 4*Q*K*L <= 4*S, and uses the fp32
@@ -145,7 +161,8 @@ MSDA_API msda_status_t msda_forward(const void *value, const int64_t *spatial_sh
 
 /* Bytes of device workspace msda_backward needs: B*S*M*D*4 for a 16-bit
  * dtype with MSDA_ACC_FP32_BUFFER, or MSDA_ACC_AUTO where it resolves to the
- * fp32 buffer, else 0. Returns 0 for
+ * fp32 buffer; B*S*M*D*2 + 20480 for bf16 with MSDA_ACC_FP16_BUFFER; else 0.
+ * Returns 0 for
  * invalid dims. */
 MSDA_API size_t msda_backward_workspace_bytes(const msda_dims_t *dims,
                                      msda_dtype_t dtype, msda_accum_t accum);

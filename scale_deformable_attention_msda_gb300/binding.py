@@ -17,7 +17,7 @@ import torch
 from . import build as _build
 
 MSDA_F32, MSDA_BF16, MSDA_F16, MSDA_F64 = 0, 1, 2, 3
-MSDA_ACC_NATIVE, MSDA_ACC_FP32_BUFFER, MSDA_ACC_AUTO = 0, 1, 2
+MSDA_ACC_NATIVE, MSDA_ACC_FP32_BUFFER, MSDA_ACC_AUTO, MSDA_ACC_FP16_BUFFER = 0, 1, 2, 3
 _DTYPES = {torch.float32: MSDA_F32, torch.bfloat16: MSDA_BF16, torch.float16: MSDA_F16,
            torch.float64: MSDA_F64}
 STATUS = {0: "MSDA_OK", 1: "MSDA_ERR_NULL", 2: "MSDA_ERR_SHAPE", 3: "MSDA_ERR_DTYPE",

@@ -14,6 +14,12 @@ cudaError_t launch_backward(const Params &p, msda_dtype_t dt, bool f32acc, int l
 cudaError_t launch_zero(void *p, int64_t bytes, cudaStream_t stream);
 cudaError_t launch_convert(const float *ws, void *gv, int64_t n, msda_dtype_t dt,
                            cudaStream_t stream);
+cudaError_t launch_f16_prepare(void *ws, int64_t n, const void *grad_out, int64_t ng,
+                               const void *attn, int64_t na, int64_t Q, int64_t LK,
+                               cudaStream_t stream);
+const float *f16_scale_pair(const void *ws, int64_t n);
+cudaError_t launch_f16_finish(const void *ws, void *gv, int64_t n, cudaStream_t stream);
+cudaError_t launch_backward_f16acc(const Params &p, int lpg, bool softmax, cudaStream_t stream);
 cudaError_t launch_corners(const Params &p, msda_dtype_t dt, int32_t *rows, cudaStream_t stream);
 cudaError_t launch_forward_f64(const Params &p, int lpg, bool softmax, cudaStream_t stream);
 cudaError_t launch_backward_f64(const Params &p, int lpg, bool softmax, cudaStream_t stream);
@@ -35,8 +41,11 @@ int elem_bytes(msda_dtype_t dt) { return dt == MSDA_F64 ? 8 : (dt == MSDA_F32 ? 
 // accumulation when the value rows receive on average at most kAutoMeanAdds
 // corner adds per head (4 Q K L <= kAutoMeanAdds S), the fp32 workspace
 // otherwise. Other modes are returned unchanged.
+// MSDA_ACC_FP16_BUFFER applies to bf16 data; other dtypes accumulate natively
+// (fp16 data already adds in fp16, fp32 and fp64 in their own type).
 constexpr int64_t kAutoMeanAdds = 4;
-msda_accum_t resolve_accum(const msda_dims_t &d, msda_accum_t accum) {
+msda_accum_t resolve_accum(const msda_dims_t &d, msda_dtype_t dt, msda_accum_t accum) {
+    if (accum == MSDA_ACC_FP16_BUFFER) return dt == MSDA_BF16 ? accum : MSDA_ACC_NATIVE;
     if (accum != MSDA_ACC_AUTO) return accum;
     const double adds = 4.0 * (double)d.Q * (double)d.K * (double)d.L;
     return adds <= (double)kAutoMeanAdds * (double)d.S ? MSDA_ACC_NATIVE : MSDA_ACC_FP32_BUFFER;
@@ -199,8 +208,11 @@ msda_status_t msda_forward_softmax(const void *value, const int64_t *spatial_sha
 size_t msda_backward_workspace_bytes(const msda_dims_t *dims, msda_dtype_t dtype,
                                      msda_accum_t accum) {
     if (check_dims(dims, dtype, nullptr) != MSDA_OK) return 0;
-    if (!is_16bit(dtype) || resolve_accum(*dims, accum) != MSDA_ACC_FP32_BUFFER) return 0;
-    return (size_t)(dims->B * dims->S * dims->M * dims->D) * sizeof(float);
+    const msda_accum_t acc = resolve_accum(*dims, dtype, accum);
+    const size_t n = (size_t)(dims->B * dims->S * dims->M * dims->D);
+    if (acc == MSDA_ACC_FP16_BUFFER) return n * 2 + msda::kF16TailBytes;
+    if (!is_16bit(dtype) || acc != MSDA_ACC_FP32_BUFFER) return 0;
+    return n * sizeof(float);
 }
 
 namespace {
@@ -209,26 +221,32 @@ namespace {
 struct BackwardPlan {
     int lpg;
     bool f32acc;      // 16-bit data accumulated in the fp32 workspace
+    bool f16acc;      // bf16 data accumulated in the scaled fp16 workspace
     void *target;     // what the atomics add into
     int64_t nval;     // B*S*M*D
     int64_t target_bytes;
 };
 
+// one_call: the scaled fp16 workspace needs grad_out in its zero step, so only
+// msda_backward and msda_backward_softmax accept it for bf16 data.
 msda_status_t plan_target(void *grad_value, void *workspace, size_t workspace_bytes,
                           msda_accum_t accum, const msda_dims_t *dims, msda_dtype_t dtype,
-                          BackwardPlan *bp) {
+                          BackwardPlan *bp, bool one_call = false) {
     msda_status_t st = check_dims(dims, dtype, &bp->lpg);
     if (st != MSDA_OK) return st;
-    if (accum != MSDA_ACC_NATIVE && accum != MSDA_ACC_FP32_BUFFER && accum != MSDA_ACC_AUTO)
+    if (accum != MSDA_ACC_NATIVE && accum != MSDA_ACC_FP32_BUFFER && accum != MSDA_ACC_AUTO &&
+        accum != MSDA_ACC_FP16_BUFFER)
         return MSDA_ERR_DTYPE;
     const msda_dims_t &d = *dims;
-    accum = resolve_accum(d, accum);
+    accum = resolve_accum(d, dtype, accum);
+    if (accum == MSDA_ACC_FP16_BUFFER && !one_call) return MSDA_ERR_DTYPE;
     bp->f32acc = is_16bit(dtype) && accum == MSDA_ACC_FP32_BUFFER;
+    bp->f16acc = accum == MSDA_ACC_FP16_BUFFER;
     bp->nval = d.B * d.S * d.M * d.D;
-    bp->target = bp->f32acc ? workspace : grad_value;
+    bp->target = (bp->f32acc || bp->f16acc) ? workspace : grad_value;
     bp->target_bytes = bp->nval * (bp->f32acc ? 4 : elem_bytes(dtype));
     if (d.B == 0) return MSDA_OK;
-    if (bp->f32acc) {
+    if (bp->f32acc || bp->f16acc) {
         const size_t need = msda_backward_workspace_bytes(dims, dtype, accum);
         if (!workspace || workspace_bytes < need) return MSDA_ERR_WORKSPACE;
         if (!aligned(workspace, 16)) return MSDA_ERR_ALIGN;
@@ -334,7 +352,8 @@ static msda_status_t backward_impl(const void *value, const int64_t *spatial_sha
                                    void *stream) {
     // Validate everything before the first launch, so that an error enqueues nothing.
     BackwardPlan bp;
-    msda_status_t st = plan_target(grad_value, workspace, workspace_bytes, accum, dims, dtype, &bp);
+    msda_status_t st = plan_target(grad_value, workspace, workspace_bytes, accum, dims, dtype, &bp,
+                                   true);
     if (st != MSDA_OK) return st;
     const msda_dims_t &d = *dims;
     if (softmax && !softmax_fits(d, dtype, bp.lpg)) return MSDA_ERR_SHAPE;
@@ -351,6 +370,31 @@ static msda_status_t backward_impl(const void *value, const int64_t *spatial_sha
         (grad_attention_weights && !aligned(grad_attention_weights, e)) ||
         (query_order && !aligned(query_order, 4)))
         return MSDA_ERR_ALIGN;
+    if (bp.f16acc) {
+        cudaStream_t s = static_cast<cudaStream_t>(stream);
+        if (d.Q == 0)   // nothing to add: grad_value is zero
+            return msda_backward_zero(grad_value, nullptr, 0, MSDA_ACC_NATIVE, dims, dtype, stream);
+        Params p = make_params(d);
+        if (msda::fault_word_for_launch(&p.err) != cudaSuccess) return MSDA_ERR_CUDA;
+        p.value = value;
+        p.shapes = spatial_shapes;
+        p.starts = level_start_index;
+        p.loc = sampling_locations;
+        p.attn = attention_weights;
+        p.order = query_order;
+        p.grad_out = grad_out;
+        p.grad_value = workspace;
+        p.acc_scale = msda::f16_scale_pair(workspace, bp.nval);
+        p.grad_loc = grad_sampling_locations;
+        p.grad_attn = grad_attention_weights;
+        // the softmax variant's weights are probabilities: no pass over the logits
+        cudaError_t e = msda::launch_f16_prepare(workspace, bp.nval, grad_out, d.B * d.Q * d.M * d.D,
+                                                 softmax ? nullptr : attention_weights,
+                                                 d.B * d.Q * d.M * d.L * d.K, d.Q, d.L * d.K, s);
+        if (e == cudaSuccess) e = msda::launch_backward_f16acc(p, bp.lpg, softmax, s);
+        if (e == cudaSuccess) e = msda::launch_f16_finish(workspace, grad_value, bp.nval, s);
+        return from_cuda(e);
+    }
     st = msda_backward_zero(grad_value, workspace, workspace_bytes, accum, dims, dtype, stream);
     if (st != MSDA_OK) return st;
     st = accumulate_impl(value, spatial_shapes, level_start_index, sampling_locations,

@@ -35,6 +35,8 @@
 // in fp32 into a workspace that a second kernel rounds into grad_value.
 #pragma once
 
+#include <type_traits>
+
 #include "msda_common.cuh"
 
 namespace msda {
@@ -93,6 +95,20 @@ template <int LPG> struct Scatter<__nv_bfloat16, false, LPG> {
     }
 };
 template <int LPG> struct Scatter<__half, false, LPG> {
+    using Acc = __half;
+    static constexpr int NSC = 8;
+    static __device__ __forceinline__ void add(__half *row, float w, const float *sc, int r) {
+        float t[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) t[i] = w * sc[i];
+        red_add_v4_f16x2(row + 8 * r, pack16<__half>(t));
+    }
+};
+
+// 16-bit data accumulated in the scaled fp16 workspace (MSDA_ACC_FP16_BUFFER):
+// lane r adds its 8 channels, with the call's scale folded into w by the
+// kernel, in one red.noftz.v4.f16x2 (64-byte groups per query-head).
+template <int LPG> struct ScatterF16 {
     using Acc = __half;
     static constexpr int NSC = 8;
     static __device__ __forceinline__ void add(__half *row, float w, const float *sc, int r) {
@@ -212,10 +228,17 @@ __device__ __forceinline__ void merge_shared_rows(float4 &w, const int4 &o, int 
 // registers and run at 3 blocks (436.9 against 422.5 us); native bf16
 // accumulation took 96 registers at 2 blocks (332 us), 80 at 3 (291 us),
 // and takes 285 us here; the fp32 softmax one 461 against 449 us.
-template <typename T, int LPG, bool F32ACC, bool SOFTMAX, bool NARROW, bool SPL>
+//
+// F16ACC (bf16 data, MSDA_ACC_FP16_BUFFER): the 16-byte-lane kernel of native
+// accumulation, adding into an fp16 workspace instead of grad_value, with every
+// contribution multiplied by *p.acc_scale (a power of two chosen per call from
+// max |grad_out|, so that sums stay inside fp16's range): fp16 keeps 11 bits
+// where bf16 keeps 8, at the same 64 bytes per add.
+template <typename T, int LPG, bool F32ACC, bool SOFTMAX, bool NARROW, bool SPL, bool F16ACC = false>
 __global__ void __launch_bounds__(kThreads, 4)
 msda_backward_kernel(const Params p) {
     static_assert(!NARROW || (F32ACC && sizeof(T) == 2), "narrow lanes: 16-bit data, fp32 workspace");
+    static_assert(!F16ACC || (!F32ACC && !NARROW && sizeof(T) == 2), "fp16 workspace: 16-bit data");
     constexpr int LB = NARROW ? 8 : 16;      // bytes of one corner vector per lane
     constexpr int VEC = LB / (int)sizeof(T);
     constexpr int GPW = 32 / LPG;
@@ -224,7 +247,7 @@ msda_backward_kernel(const Params p) {
     constexpr int NP = SPW / 32;             // samples each lane prepares per chunk
     constexpr int UW = NARROW ? 2 : 1;       // samples gathered at a time
     constexpr int U = CH < UW ? CH : UW;
-    using S = Scatter<T, F32ACC, LPG>;
+    using S = std::conditional_t<F16ACC, ScatterF16<LPG>, Scatter<T, F32ACC, LPG>>;
     using Acc = typename S::Acc;
     constexpr int NSC = NARROW ? VEC : S::NSC;
 
@@ -275,6 +298,8 @@ msda_backward_kernel(const Params p) {
 #pragma unroll
         for (int i = 0; i < NSC; ++i) sc[i] = 0.0f;
     }
+    // fp16 workspace: the call's scale, folded into each corner's weight
+    const float acc_scale = F16ACC ? *p.acc_scale : 1.0f;
 
     // phase-1/3 mapping as in the forward: slot lane + 32*i is chunk sample
     // pj + i*LPG of group pg = lane % GPW, i.e. sample ((pj + i*LPG) << sl2)
@@ -390,7 +415,7 @@ msda_backward_kernel(const Params p) {
                         float *dst = reinterpret_cast<float *>(gvhead) + oc[c] + 4 * r;
                         red_add_v4_f32(dst, wc[c] * sc[0], wc[c] * sc[1], wc[c] * sc[2], wc[c] * sc[3]);
                     } else {
-                        S::add(gvhead + oc[c], wc[c], sc, r);
+                        S::add(gvhead + oc[c], F16ACC ? wc[c] * acc_scale : wc[c], sc, r);
                     }
                 }
 #pragma unroll
@@ -454,7 +479,7 @@ msda_backward_kernel(const Params p) {
     }
 }
 
-template <typename T, bool F32ACC, bool SOFTMAX, bool SPL>
+template <typename T, bool F32ACC, bool SOFTMAX, bool SPL, bool F16ACC = false>
 static cudaError_t launch_backward_t(const Params &p, int lpg, cudaStream_t stream) {
     // 16-bit data with the fp32 workspace: twice the lanes, 8 bytes each
     constexpr bool kNarrowable = F32ACC && sizeof(T) == 2;
@@ -466,7 +491,7 @@ static cudaError_t launch_backward_t(const Params &p, int lpg, cudaStream_t stre
     if (blocks == 0) return cudaSuccess;
     if (blocks > 0x7fffffff) return cudaErrorInvalidConfiguration;
     const dim3 grid((unsigned)blocks);
-#define MSDA_BWD(N, NAR) msda_backward_kernel<T, N, F32ACC, SOFTMAX, NAR, SPL><<<grid, kThreads, 0, stream>>>(p)
+#define MSDA_BWD(N, NAR) msda_backward_kernel<T, N, F32ACC, SOFTMAX, NAR, SPL, F16ACC><<<grid, kThreads, 0, stream>>>(p)
     if constexpr (kNarrowable) {
         if (narrow) {
             switch (lanes) {
@@ -507,6 +532,14 @@ static cudaError_t launch_backward_s(const Params &p, msda_dtype_t dt, bool f32a
     }
     return cudaErrorInvalidValue;
 }
+
+// bf16 data with the scaled fp16 workspace (msda_backward_f16acc.cu): the
+// native kernel's lanes adding fp16; p.split_log2 already chosen.
+template <bool SOFTMAX, bool SPL>
+static cudaError_t launch_backward_f16acc_s(const Params &p, int lpg, cudaStream_t stream) {
+    return launch_backward_t<__nv_bfloat16, false, SOFTMAX, SPL, true>(p, lpg, stream);
+}
+cudaError_t launch_backward_f16acc(const Params &p, int lpg, bool softmax, cudaStream_t stream);
 
 // The split instantiations (msda_backward_split.cu), compiled apart so that
 // the two halves build in parallel.

@@ -18,6 +18,12 @@ namespace msda {
 constexpr int kMaxLevels = 16;
 constexpr int kWarpsPerBlock = 8;
 constexpr int kThreads = kWarpsPerBlock * 32;
+// The scaled fp16 workspace (MSDA_ACC_FP16_BUFFER) is n halfs followed by a
+// tail of kF16TailBytes: per-block maxima of |grad_out| and of |attention
+// weight| (kF16MaxBlocks floats each), then the pair (2^k, 2^-k).
+constexpr int kF16MaxBlocks = 152 * 16;
+constexpr size_t kF16TailBytes = 20480;
+static_assert((2 * kF16MaxBlocks + 2) * sizeof(float) <= kF16TailBytes, "fp16 workspace tail");
 
 // Everything a kernel needs, passed by value.
 struct Params {
@@ -29,7 +35,8 @@ struct Params {
     const int32_t *order;  // NULL: linear dispatch
     const void *grad_out;
     void *out;             // forward output
-    void *grad_value;      // fp32 workspace or the 16-bit/fp32 grad_value
+    void *grad_value;      // fp32 or fp16 workspace, or the 16-bit/fp32 grad_value
+    const float *acc_scale;  // fp16 workspace: the factor contributions are scaled by
     void *grad_loc;
     void *grad_attn;
     int B, S, Q, M, D, L, K;

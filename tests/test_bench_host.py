@@ -52,6 +52,24 @@ def test_argument_rules():
         bench.parse_args(["--warmup", "2"])
 
 
+def test_accumulator_names():
+    """The accumulator a backward resolves to and the arithmetic dtype the
+    bench line reports for it."""
+    sys.path.insert(0, ROOT)
+    import bench
+    r = bench.resolved_accumulator
+    assert r("f32", "native", 0) == "fp32_buffer"
+    assert r("bf16", "fp16_buffer", 1 << 20) == "fp16_buffer"
+    assert r("f16", "fp16_buffer", 0) == "native"
+    assert r("bf16", "auto", 0) == "native" and r("bf16", "auto", 64) == "fp32_buffer"
+    assert r("bf16", "fp32_buffer", 64) == "fp32_buffer" and r("bf16", "native", 0) == "native"
+    d = bench.arithmetic_dtype
+    assert d("f32", "fp32_buffer") == "f32" and d("bf16", "fp32_buffer") == "f32"
+    assert d("bf16", "fp16_buffer") == "f16" and d("bf16", "native") == "bf16"
+    assert set(bench.ACCUM_MODES) == {"fp32_buffer", "native", "auto", "fp16_buffer"}
+    assert bench.parse_args(["--accum", "fp16_buffer"]).accum == "fp16_buffer"
+
+
 def test_traffic_figure_needs_matching_kernel_sources(tmp_path):
     sys.path.insert(0, ROOT)
     import bench

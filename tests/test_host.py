@@ -197,8 +197,27 @@ def test_auto_accumulation_is_resolved_from_the_sizes(so):
     assert _bwd(so, dec, dtype=1, accum=2, grad_value=None) == 1  # native: no workspace asked
     assert so.msda_backward_zero(vp(FAKE), vp(None), ctypes.c_size_t(0), 2, ctypes.byref(enc),
                                  1, vp(0)) == 5
-    assert _bwd(so, enc, dtype=1, accum=3) == 3                   # unknown mode
+    assert _bwd(so, enc, dtype=1, accum=4) == 3                   # unknown mode
     assert _bwd(so, _dims(B=0), dtype=1, accum=2) == 0            # empty: nothing launched
+
+
+def test_fp16_buffer_accumulation_rules(so):
+    """MSDA_ACC_FP16_BUFFER: bf16 data needs B*S*M*D*2 + 20480 bytes and is
+    taken only by the one-call backward (its zero step reads grad_out); other
+    dtypes accumulate natively and need nothing (no CUDA call here)."""
+    vp = ctypes.c_void_p
+    d = _dims()
+    n = 2 * 22223 * 8 * 32
+    assert so.msda_backward_workspace_bytes(ctypes.byref(d), 1, 3) == 2 * n + 20480
+    assert so.msda_backward_workspace_bytes(ctypes.byref(d), 2, 3) == 0      # fp16 data
+    assert so.msda_backward_workspace_bytes(ctypes.byref(d), 0, 3) == 0      # fp32 data
+    assert so.msda_backward_zero(vp(FAKE), vp(FAKE), ctypes.c_size_t(2 * n + 20480), 3,
+                                 ctypes.byref(d), 1, vp(0)) == 3
+    assert so.msda_backward_finish(vp(FAKE), ctypes.c_size_t(2 * n + 20480), vp(FAKE), 3,
+                                   ctypes.byref(d), 1, vp(0)) == 3
+    assert _bwd(so, d, dtype=1, accum=3, ws=None) == 5
+    assert _bwd(so, d, dtype=1, accum=3, ws_bytes=2 * n + 20479) == 5
+    assert _bwd(so, _dims(B=0), dtype=1, accum=3) == 0
 
 
 def test_binding_refuses_cpu_tensors(so):
