@@ -101,9 +101,10 @@ typedef enum {
  * samples that reach it (bilinear weight w <= 1, one sample per query, level
  * and point at most), so no sum exceeds max|grad_out| * Q * A, with A = 1 for
  * msda_backward_softmax (probabilities) and L * K * max|attention weight|
- * otherwise; 2^k puts that bound in [2^14, 2^15), below fp16's largest finite
- * value, whatever the inputs. Sums below 2^-29 of the bound fall into fp16's
- * subnormals and keep fewer bits. The adds move 64 bytes per corner and head,
+ * otherwise; 2^k puts that bound below 2^15 (and, for normal inputs, at or
+ * above 2^11), under fp16's largest finite value, for any bound up to 2^141.
+ * Sums far below the bound (2^-25 of it and less) fall into fp16's subnormals
+ * and keep fewer bits. The adds move 64 bytes per corner and head,
  * as native accumulation does (half the fp32 buffer's).
  * Workspace: B*S*M*D*2 + 20480 bytes (msda_backward_workspace_bytes). For
  * fp16, fp32 and fp64 data it is the same as MSDA_ACC_NATIVE. */

@@ -14,11 +14,11 @@ cudaError_t launch_backward(const Params &p, msda_dtype_t dt, bool f32acc, int l
 cudaError_t launch_zero(void *p, int64_t bytes, cudaStream_t stream);
 cudaError_t launch_convert(const float *ws, void *gv, int64_t n, msda_dtype_t dt,
                            cudaStream_t stream);
+int f16_prepare_blocks(int64_t n, int64_t ng, const void *attn, int64_t na);
 cudaError_t launch_f16_prepare(void *ws, int64_t n, const void *grad_out, int64_t ng,
-                               const void *attn, int64_t na, int64_t Q, int64_t LK,
-                               cudaStream_t stream);
-const float *f16_scale_pair(const void *ws, int64_t n);
-cudaError_t launch_f16_finish(const void *ws, void *gv, int64_t n, cudaStream_t stream);
+                               const void *attn, int64_t na, cudaStream_t stream);
+float *f16_scale_pair(void *ws, int64_t n);
+cudaError_t launch_f16_finish(void *ws, void *gv, int64_t n, cudaStream_t stream);
 cudaError_t launch_backward_f16acc(const Params &p, int lpg, bool softmax, cudaStream_t stream);
 cudaError_t launch_corners(const Params &p, msda_dtype_t dt, int32_t *rows, cudaStream_t stream);
 cudaError_t launch_forward_f64(const Params &p, int lpg, bool softmax, cudaStream_t stream);
@@ -384,13 +384,16 @@ static msda_status_t backward_impl(const void *value, const int64_t *spatial_sha
         p.order = query_order;
         p.grad_out = grad_out;
         p.grad_value = workspace;
-        p.acc_scale = msda::f16_scale_pair(workspace, bp.nval);
+        // the softmax variant's weights are probabilities: no pass over the logits
+        const void *amax_of = softmax ? nullptr : attention_weights;
+        const int64_t ng = d.B * d.Q * d.M * d.D, na = d.B * d.Q * d.M * d.L * d.K;
+        p.f16_nmax = msda::f16_prepare_blocks(bp.nval, ng, amax_of, na);
+        p.f16_amax = amax_of != nullptr;
+        p.f16_max = reinterpret_cast<const float *>(static_cast<char *>(workspace) + bp.nval * 2);
+        p.f16_scale = msda::f16_scale_pair(workspace, bp.nval);
         p.grad_loc = grad_sampling_locations;
         p.grad_attn = grad_attention_weights;
-        // the softmax variant's weights are probabilities: no pass over the logits
-        cudaError_t e = msda::launch_f16_prepare(workspace, bp.nval, grad_out, d.B * d.Q * d.M * d.D,
-                                                 softmax ? nullptr : attention_weights,
-                                                 d.B * d.Q * d.M * d.L * d.K, d.Q, d.L * d.K, s);
+        cudaError_t e = msda::launch_f16_prepare(workspace, bp.nval, grad_out, ng, amax_of, na, s);
         if (e == cudaSuccess) e = msda::launch_backward_f16acc(p, bp.lpg, softmax, s);
         if (e == cudaSuccess) e = msda::launch_f16_finish(workspace, grad_value, bp.nval, s);
         return from_cuda(e);

@@ -26,80 +26,70 @@ __global__ void convert8_kernel(const float4 *ws, uint4 *gv, int64_t n8) {
 
 // Scaled fp16 workspace (MSDA_ACC_FP16_BUFFER), before the adds: zero the
 // workspace and record each block's largest |grad_out| (bf16, 8 per word) and,
-// when attn is given, its largest |attention weight| (bf16, one at a time: the
-// weights are 2-byte aligned only).
-__device__ __forceinline__ float block_max_of(float m, float *warp_max) {
+// when attn is given, its largest |attention weight| (bf16; 8 per word when
+// the weights are 16-byte aligned, else one at a time). One block of 1024
+// threads per SM at most (kF16MaxBlocks), four loads in flight per thread.
+__device__ __forceinline__ float abs_max8_bf16(float m, const uint4 w) {
+    const uint32_t u[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
-    if ((threadIdx.x & 31) == 0) warp_max[threadIdx.x >> 5] = m;
-    __syncthreads();
-    float b = 0.0f;
-    for (int w = 0; w < (int)(blockDim.x >> 5); ++w) b = fmaxf(b, warp_max[w]);
-    __syncthreads();
-    return b;
+    for (int k = 0; k < 4; ++k)   // |bf16| as fp32: drop the sign, widen exactly
+        m = fmaxf(m, fmaxf(__uint_as_float((u[k] << 16) & 0x7fffffffu),
+                           __uint_as_float(u[k] & 0x7fff0000u)));
+    return m;
+}
+
+__device__ __forceinline__ float abs_max_stream(float m, const uint4 *x, int64_t n8, int64_t i0,
+                                                int64_t stride) {
+    int64_t i = i0;
+    for (; i + 3 * stride < n8; i += 4 * stride) {
+        const uint4 a = x[i], b = x[i + stride], c = x[i + 2 * stride], d = x[i + 3 * stride];
+        m = abs_max8_bf16(abs_max8_bf16(abs_max8_bf16(abs_max8_bf16(m, a), b), c), d);
+    }
+    for (; i < n8; i += stride) m = abs_max8_bf16(m, x[i]);
+    return m;
 }
 
 __global__ void zero_f16_max_kernel(uint4 *ws, int64_t n16, const uint4 *gout, int64_t ng8,
                                     const unsigned short *attn, int64_t na, float *gmax,
                                     float *amax) {
-    __shared__ float warp_max[32];
+    __shared__ float warp_max[2][32];
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
     const int64_t i0 = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     for (int64_t i = i0; i < n16; i += stride) ws[i] = make_uint4(0u, 0u, 0u, 0u);
-    float m = 0.0f;
-    for (int64_t i = i0; i < ng8; i += stride) {
-        const uint4 w = gout[i];
-        const uint32_t u[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-        for (int k = 0; k < 4; ++k)   // |bf16| as fp32: drop the sign, widen exactly
-            m = fmaxf(m, fmaxf(__uint_as_float((u[k] << 16) & 0x7fffffffu),
-                               __uint_as_float(u[k] & 0x7fff0000u)));
-    }
+    float m = abs_max_stream(0.0f, gout, ng8, i0, stride);
     float ma = 0.0f;
-    if (attn)
-        for (int64_t i = i0; i < na; i += stride)
-            ma = fmaxf(ma, __uint_as_float(((uint32_t)attn[i] << 16) & 0x7fffffffu));
-    m = block_max_of(m, warp_max);
-    ma = block_max_of(ma, warp_max);
-    if (threadIdx.x == 0) {
-        gmax[blockIdx.x] = m;
-        amax[blockIdx.x] = ma;
-    }
-}
-
-// One block: the call's scale 2^k. Every element of grad_value sums, over the
-// samples that reach it, |a| * w * |g| with bilinear weight w <= 1, one sample
-// per (q, l, k) at most, so |sum| <= max|g| * Q * A, where A = max over
-// query-heads of sum_{l,k} |a| <= L K max|a| (A = 1 for the softmax variant,
-// whose weights are probabilities). k puts that bound in [2^14, 2^15): no sum
-// can pass fp16's largest finite value, 65504. Inside fp16's normal range the
-// rounding of a sum does not depend on k; a sum below 2^-29 of the bound falls
-// into fp16's subnormals and keeps fewer bits.
-__global__ void f16_scale_kernel(const float *gmax, const float *amax, int n, int64_t Q,
-                                 int64_t LK, float *scale_pair) {
-    __shared__ float warp_max[32];
-    float m = 0.0f, ma = 0.0f;
-    for (int i = threadIdx.x; i < n; i += blockDim.x) {
-        m = fmaxf(m, gmax[i]);
-        if (amax) ma = fmaxf(ma, amax[i]);
-    }
-    m = block_max_of(m, warp_max);
-    ma = block_max_of(ma, warp_max);
-    if (threadIdx.x == 0) {
-        const double a = amax ? (double)LK * (double)ma : 1.0;
-        const double bound = (double)m * (double)Q * a;
-        int k = 0;
-        if (bound > 0.0 && bound < 1.0e300) {
-            int e;
-            (void)frexp(bound, &e);              // bound = f 2^e, f in [0.5, 1)
-            k = min(max(15 - e, -126), 126);
+    if (attn) {
+        int64_t done = 0;
+        if ((reinterpret_cast<uintptr_t>(attn) & 15u) == 0) {
+            ma = abs_max_stream(ma, reinterpret_cast<const uint4 *>(attn), na / 8, i0, stride);
+            done = na / 8 * 8;
         }
-        scale_pair[0] = ldexpf(1.0f, k);
-        scale_pair[1] = ldexpf(1.0f, -k);
+        for (int64_t i = done + i0; i < na; i += stride)
+            ma = fmaxf(ma, __uint_as_float(((uint32_t)attn[i] << 16) & 0x7fffffffu));
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+        m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+        ma = fmaxf(ma, __shfl_xor_sync(0xffffffffu, ma, off));
+    }
+    if ((threadIdx.x & 31) == 0) {
+        warp_max[0][threadIdx.x >> 5] = m;
+        warp_max[1][threadIdx.x >> 5] = ma;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        float b = 0.0f, ba = 0.0f;
+        for (int w = 0; w < (int)(blockDim.x >> 5); ++w) {
+            b = fmaxf(b, warp_max[0][w]);
+            ba = fmaxf(ba, warp_max[1][w]);
+        }
+        gmax[blockIdx.x] = b;
+        amax[blockIdx.x] = ba;
     }
 }
 
-// After the adds: grad_value = round(workspace * 2^-k), 8 elements per thread.
+// After the adds: grad_value = round(workspace * 2^-k), 8 elements per thread;
+// (2^k, 2^-k) as block 0 of the backward stored it.
 template <typename T>
 __global__ void finish_f16_kernel(const uint4 *ws, uint4 *gv, int64_t n8, const float *scale_pair) {
     const float inv = scale_pair[1];
@@ -113,13 +103,9 @@ __global__ void finish_f16_kernel(const uint4 *ws, uint4 *gv, int64_t n8, const 
     }
 }
 
-// a few waves of resident blocks on 152 SMs; the fp16 workspace's tail holds
-// one maximum per block of such a grid
-constexpr int64_t kStreamGridCap = 152 * 16;
-static_assert(kStreamGridCap <= kF16MaxBlocks, "fp16 workspace tail");
 static unsigned stream_grid(int64_t n, int threads) {
     const int64_t want = (n + threads - 1) / threads;
-    const int64_t cap = kStreamGridCap;
+    const int64_t cap = 152 * 16;  // a few waves of resident blocks on 152 SMs
     return (unsigned)(want < 1 ? 1 : (want < cap ? want : cap));
 }
 
@@ -146,28 +132,29 @@ cudaError_t launch_convert(const float *ws, void *gv, int64_t n, msda_dtype_t dt
 }
 
 // The scaled fp16 workspace: [accumulator: n halfs][tail], the tail laid out
-// as kF16MaxBlocks says. Zero + maxima, scale, (adds), finish. attn NULL: the
-// weights are probabilities (the softmax variant).
-cudaError_t launch_f16_prepare(void *ws, int64_t n, const void *grad_out, int64_t ng,
-                               const void *attn, int64_t na, int64_t Q, int64_t LK,
-                               cudaStream_t stream) {
-    const int64_t n16 = n * 2 / 16, ng8 = ng / 8;
-    float *tail = reinterpret_cast<float *>(static_cast<char *>(ws) + n * 2);
-    int64_t work = n16 > ng8 ? n16 : ng8;
+// as kF16MaxBlocks says. Zero + maxima here; the backward derives the scale
+// from the maxima (f16_block_scale) and the finish pass applies its inverse.
+// attn NULL: the weights are probabilities (the softmax variant).
+int f16_prepare_blocks(int64_t n, int64_t ng, const void *attn, int64_t na) {
+    int64_t work = n / 8 > ng / 8 ? n / 8 : ng / 8;
     if (attn && na / 8 > work) work = na / 8;
-    const unsigned grid = stream_grid(work, 256);   // <= kF16MaxBlocks
-    zero_f16_max_kernel<<<grid, 256, 0, stream>>>(reinterpret_cast<uint4 *>(ws), n16,
-                                                  reinterpret_cast<const uint4 *>(grad_out), ng8,
+    const int64_t want = (work + 1023) / 1024;
+    return (int)(want < 1 ? 1 : (want < kF16MaxBlocks ? want : kF16MaxBlocks));
+}
+cudaError_t launch_f16_prepare(void *ws, int64_t n, const void *grad_out, int64_t ng,
+                               const void *attn, int64_t na, cudaStream_t stream) {
+    float *tail = reinterpret_cast<float *>(static_cast<char *>(ws) + n * 2);
+    const int grid = f16_prepare_blocks(n, ng, attn, na);
+    zero_f16_max_kernel<<<grid, 1024, 0, stream>>>(reinterpret_cast<uint4 *>(ws), n * 2 / 16,
+                                                  reinterpret_cast<const uint4 *>(grad_out), ng / 8,
                                                   static_cast<const unsigned short *>(attn), na,
-                                                  tail, tail + kF16MaxBlocks);
-    f16_scale_kernel<<<1, 256, 0, stream>>>(tail, attn ? tail + kF16MaxBlocks : nullptr, (int)grid,
-                                            Q, LK, tail + 2 * kF16MaxBlocks);
+                                                  tail, tail + grid);
     return cudaGetLastError();
 }
-const float *f16_scale_pair(const void *ws, int64_t n) {
-    return reinterpret_cast<const float *>(static_cast<const char *>(ws) + n * 2) + 2 * kF16MaxBlocks;
+float *f16_scale_pair(void *ws, int64_t n) {
+    return reinterpret_cast<float *>(static_cast<char *>(ws) + n * 2) + 2 * kF16MaxBlocks;
 }
-cudaError_t launch_f16_finish(const void *ws, void *gv, int64_t n, cudaStream_t stream) {
+cudaError_t launch_f16_finish(void *ws, void *gv, int64_t n, cudaStream_t stream) {
     const int64_t n8 = n / 8;
     if (n8 == 0) return cudaSuccess;
     finish_f16_kernel<__nv_bfloat16><<<stream_grid(n8, 256), 256, 0, stream>>>(

@@ -119,6 +119,78 @@ template <int LPG> struct ScatterF16 {
     }
 };
 
+// The scale 2^k of the fp16 workspace. Every element of grad_value sums, over
+// the samples that reach it, |a| * w * |g| with bilinear weight w <= 1 and one
+// sample per (q, l, k) at most, so |sum| <= max|g| * Q * A, where A = max over
+// query-heads of sum_{l,k} |a| <= L K max|a| (A = 1 for the softmax variant,
+// whose weights are probabilities). With each factor x < 2^e(x), k = 15 -
+// sum of the e's puts that bound below 2^15, under fp16's largest finite
+// value, 65504 (and, for normal inputs, at or above 2^11), for any bound up
+// to 2^141. Inside fp16's normal range the rounding of a sum does not depend
+// on k; a sum below 2^-25 of the bound falls into fp16's subnormals and keeps
+// fewer bits. Integer arithmetic only: every
+// thread of every block evaluates it. A zero or non-finite maximum gives k = 0.
+__device__ __forceinline__ int exp_above(float x) {      // x < 2^e for 0 < x < inf
+    return (int)((__float_as_uint(x) >> 23) & 0xffu) - 126;
+}
+__device__ __forceinline__ int exp_above(int64_t x) {    // x < 2^e for x >= 1
+    return 64 - __clzll((long long)x);
+}
+__device__ __forceinline__ float f16_scale_of(float gmax, float amax, bool have_amax, int64_t Q,
+                                              int64_t LK) {
+    const bool finite = gmax > 0.0f && gmax <= 3.4028235e38f &&
+                        (!have_amax || (amax > 0.0f && amax <= 3.4028235e38f));
+    int e = exp_above(gmax) + exp_above(Q < 1 ? (int64_t)1 : Q);
+    if (have_amax) e += exp_above(amax) + exp_above(LK < 1 ? (int64_t)1 : LK);
+    const int k = finite ? min(max(15 - e, -126), 126) : 0;
+    return __uint_as_float((uint32_t)(k + 127) << 23);  // 2^k, a normal float
+}
+
+__device__ __forceinline__ void f16_warp_store(float m, float ma, float *s) {
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+        m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+        ma = fmaxf(ma, __shfl_xor_sync(0xffffffffu, ma, off));
+    }
+    if ((threadIdx.x & 31) == 0) {
+        s[threadIdx.x >> 5] = m;
+        s[kWarpsPerBlock + (threadIdx.x >> 5)] = ma;
+    }
+}
+
+// Each warp's maximum over the prepare pass's block maxima into s[warp] (of
+// |grad_out|) and s[kWarpsPerBlock + warp] (of |attention weight|). The
+// 2 * f16_nmax <= 2 * kF16MaxBlocks values take at most two loads per thread,
+// both in flight with the level table's.
+static_assert(2 * kF16MaxBlocks <= 2 * kThreads, "two loads per thread");
+__device__ __forceinline__ void f16_warp_maxima(const Params &p, float *s) {
+    const int n = p.f16_nmax, total = p.f16_amax ? 2 * n : n;
+    const int j0 = threadIdx.x, j1 = threadIdx.x + kThreads;
+    const float v0 = j0 < total ? p.f16_max[j0] : 0.0f;
+    const float v1 = j1 < total ? p.f16_max[j1] : 0.0f;
+    const float m = fmaxf(j0 < n ? v0 : 0.0f, j1 < n ? v1 : 0.0f);
+    const float ma = fmaxf(j0 >= n ? v0 : 0.0f, j1 >= n ? v1 : 0.0f);
+    f16_warp_store(m, ma, s);
+}
+
+// After a __syncthreads that follows f16_warp_maxima: the call's 2^k; block 0
+// stores (2^k, 2^-k) for the finish pass.
+__device__ __forceinline__ float f16_block_scale(const Params &p, const float *s) {
+    float m = 0.0f, ma = 0.0f;
+#pragma unroll
+    for (int w = 0; w < kWarpsPerBlock; ++w) {
+        m = fmaxf(m, s[w]);
+        ma = fmaxf(ma, s[kWarpsPerBlock + w]);
+    }
+    const float scale = f16_scale_of(m, ma, p.f16_amax != 0, p.Q, p.LK);
+    if (blockIdx.x == 0 && threadIdx.x == 0) {
+        p.f16_scale[0] = scale;
+        p.f16_scale[1] = __uint_as_float((uint32_t)(254 - ((__float_as_uint(scale) >> 23) & 0xffu))
+                                         << 23);  // 2^-k
+    }
+    return scale;
+}
+
 // 8 bytes of T (4 channels) as fp32.
 template <typename T> __device__ __forceinline__ void load4(float *v, const T *p) {
     const uint2 u = __ldg(reinterpret_cast<const uint2 *>(p));
@@ -231,9 +303,9 @@ __device__ __forceinline__ void merge_shared_rows(float4 &w, const int4 &o, int 
 //
 // F16ACC (bf16 data, MSDA_ACC_FP16_BUFFER): the 16-byte-lane kernel of native
 // accumulation, adding into an fp16 workspace instead of grad_value, with every
-// contribution multiplied by *p.acc_scale (a power of two chosen per call from
-// max |grad_out|, so that sums stay inside fp16's range): fp16 keeps 11 bits
-// where bf16 keeps 8, at the same 64 bytes per add.
+// contribution multiplied by 2^k (f16_scale_of; each block derives it from the
+// prepare pass's block maxima while it loads the level table): fp16 keeps 11
+// bits where bf16 keeps 8, at the same 64 bytes per add.
 template <typename T, int LPG, bool F32ACC, bool SOFTMAX, bool NARROW, bool SPL, bool F16ACC = false>
 __global__ void __launch_bounds__(kThreads, 4)
 msda_backward_kernel(const Params p) {
@@ -256,10 +328,14 @@ msda_backward_kernel(const Params p) {
     __shared__ int4 s_o[kWarpsPerBlock][SPW];
     __shared__ float4 s_dot[kWarpsPerBlock][SPW];
     __shared__ float s_ga[kWarpsPerBlock][SOFTMAX ? kSoftmaxSlots : 1];
+    __shared__ float s_f16max[F16ACC ? 2 * kWarpsPerBlock : 1];
     constexpr int SLOTS = SOFTMAX ? kSoftmaxSlots / GPW : 1;   // samples per query-head
 
     load_level_table(lt, p);
+    if constexpr (F16ACC) f16_warp_maxima(p, s_f16max);
     __syncthreads();
+    // fp16 workspace: the call's scale, folded into each corner's weight
+    const float acc_scale = F16ACC ? f16_block_scale(p, s_f16max) : 1.0f;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g = lane / LPG, r = lane % LPG;
@@ -298,9 +374,6 @@ msda_backward_kernel(const Params p) {
 #pragma unroll
         for (int i = 0; i < NSC; ++i) sc[i] = 0.0f;
     }
-    // fp16 workspace: the call's scale, folded into each corner's weight
-    const float acc_scale = F16ACC ? *p.acc_scale : 1.0f;
-
     // phase-1/3 mapping as in the forward: slot lane + 32*i is chunk sample
     // pj + i*LPG of group pg = lane % GPW, i.e. sample ((pj + i*LPG) << sl2)
     // + psub of the chunk of query-head t0 + (pg >> sl2)

@@ -21,7 +21,7 @@ constexpr int kThreads = kWarpsPerBlock * 32;
 // The scaled fp16 workspace (MSDA_ACC_FP16_BUFFER) is n halfs followed by a
 // tail of kF16TailBytes: per-block maxima of |grad_out| and of |attention
 // weight| (kF16MaxBlocks floats each), then the pair (2^k, 2^-k).
-constexpr int kF16MaxBlocks = 152 * 16;
+constexpr int kF16MaxBlocks = 152;
 constexpr size_t kF16TailBytes = 20480;
 static_assert((2 * kF16MaxBlocks + 2) * sizeof(float) <= kF16TailBytes, "fp16 workspace tail");
 
@@ -36,7 +36,12 @@ struct Params {
     const void *grad_out;
     void *out;             // forward output
     void *grad_value;      // fp32 or fp16 workspace, or the 16-bit/fp32 grad_value
-    const float *acc_scale;  // fp16 workspace: the factor contributions are scaled by
+    // fp16 workspace: per-block maxima of |grad_out| (f16_nmax of them, then as
+    // many of |attention weight| when f16_amax), and where block 0 of the
+    // backward stores the call's (2^k, 2^-k) for the finish pass
+    const float *f16_max;
+    float *f16_scale;
+    int f16_nmax, f16_amax;
     void *grad_loc;
     void *grad_attn;
     int B, S, Q, M, D, L, K;
