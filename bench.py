@@ -54,6 +54,9 @@ def parse_args(argv=None):
     ap.add_argument("--accum", default="fp32_buffer", choices=["fp32_buffer", "native", "auto", "fp16_buffer"])
     ap.add_argument("--no-f32-line", action="store_true",
                     help="skip the second timed phase with fp32 storage (the line's f32_encoder)")
+    ap.add_argument("--no-accum-lines", action="store_true",
+                    help="skip the timed phases of the other 16-bit accumulators (the line's "
+                         "accumulator_modes)")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=50)
@@ -194,6 +197,13 @@ ACCUM_MODES = {"fp32_buffer": lambda b: b.MSDA_ACC_FP32_BUFFER,
                "fp16_buffer": lambda b: b.MSDA_ACC_FP16_BUFFER}
 
 
+# Kernels one bench step launches, by the accumulator the backward resolved to:
+# forward, zero (grad_value or workspace), accumulate, finish (16-bit data with
+# the fp32 workspace); fp32 data and native 16-bit adds need no finish; the
+# fp16 workspace's one call: zero + maxima, accumulate, finish.
+LAUNCHES_PER_STEP = {"fp32_buffer": 4, "native": 3, "fp16_buffer": 4, "f32": 3}
+
+
 def arithmetic_dtype(storage: str, resolved: str) -> str:
     """The type the step's arithmetic and grad_value accumulation run in:
     fp32 for fp32 storage and for 16-bit storage with the fp32 workspace; fp16
@@ -244,6 +254,8 @@ PROFILE_FILES = {
     ("msda_forward_kernel", "bf16", "native"): "msda_forward_kernel_encoder.md",
     ("msda_backward_kernel", "bf16", "fp32_buffer"): "msda_backward_kernel_encoder.md",
     ("msda_backward_kernel", "bf16", "native"): "msda_backward_kernel_native_encoder.md",
+    ("msda_forward_kernel", "bf16", "fp16_buffer"): "msda_forward_kernel_encoder.md",
+    ("msda_backward_kernel", "bf16", "fp16_buffer"): "msda_backward_kernel_fp16_buffer_encoder.md",
     ("msda_forward_kernel", "f32", "fp32_buffer"): "msda_kernels_f32_encoder.md",
     ("msda_backward_kernel", "f32", "fp32_buffer"): "msda_kernels_f32_encoder.md",
 }
@@ -518,8 +530,8 @@ def run_ours(args):
                                    "valid while the kernel sources hash as recorded there)")
                 if traffic is not None else "none: no ncu summary of this kernel's current code"}
         if acc_name == "fp16_buffer" and dominant == "backward":
-            roof["duration_covers"] = ("the one msda_backward call: zero + maxima, scale, the "
-                                       "kernel, finish")
+            roof["duration_covers"] = ("the one msda_backward call: zero + maxima, the kernel, "
+                                       "finish")
         kernels = {}
         for n in names:
             k = {"ms": round(mean[n], 5)}
@@ -565,6 +577,28 @@ def run_ours(args):
                     "step": "msda_forward + msda_backward (zero, accumulate; fp32 data needs no "
                             "finish pass)"}
         del op32
+
+    # ---- the same bf16 step with the other grad_value accumulators (the
+    # accumulator switch measured in one run); fewer steps
+    modes = None
+    if args.dtype == "bf16" and not args.no_accum_lines:
+        modes = {}
+        for name in ("fp32_buffer", "native", "fp16_buffer"):
+            if name == acc_name:
+                continue
+            steps_m = max(1, min(args.steps, 500))
+            per_m, step_m, res_m = timed(op, ACCUM_MODES[name](binding), name, steps_m, args.warmup)
+            qps_m, slow_m, _ = job_throughput(w.B * w.Q * steps_m, sum(step_m) / 1e3, dev)
+            mean_m = {n: statistics.fmean(v) for n, v in per_m.items()}
+            modes[name] = {"value": round(qps_m, 1), "unit": UNIT, "steps": steps_m,
+                           "ms_per_step": round(slow_m * 1e3 / steps_m, 5),
+                           "dtype": arithmetic_dtype("bf16", res_m),
+                           "accumulator_resolved": res_m,
+                           "kernels_ms": {n: round(mean_m[n], 5) for n in names},
+                           "gpu_launches": LAUNCHES_PER_STEP[res_m] * steps_m}
+        modes["note"] = ("same encoder step and inputs, bf16 storage; grad_value error against "
+                         "the fp64 oracle is measured by the GPU tests, not here; fp16_buffer's "
+                         "backward is one msda_backward call (zero and finish inside it)")
     clocks = sampler.stop() if sampler else None
 
     # ---- end to end through the public API, host buffers, copies timed.
@@ -616,10 +650,7 @@ def run_ours(args):
         cpu = None
         if world == 1 and not args.no_cpu_baseline:
             cpu = cpu_baseline(p)
-        # forward, zero (grad_value and/or workspace), accumulate, finish; the
-        # fp16 workspace: forward, zero + maxima, scale, accumulate, finish
-        launches_per_step = {"fp16_buffer": 5}.get(
-            acc_name, 4 if (args.dtype != "f32" and acc_name == "fp32_buffer") else 3)
+        launches_per_step = LAUNCHES_PER_STEP["f32" if args.dtype == "f32" else acc_name]
         result = {
             "metric": METRIC, "value": round(qps, 1), "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
@@ -634,7 +665,7 @@ def run_ours(args):
                        "l2": "flushed between timed steps (256 MiB write, outside the events)",
                        "step": "msda_forward + msda_backward (zero, accumulate, finish)"
                                if acc_name != "fp16_buffer" else
-                               "msda_forward + msda_backward (one call: zero + maxima, scale, "
+                               "msda_forward + msda_backward (one call: zero + maxima, "
                                "accumulate, finish)"},
             "step_hbm": {"compulsory_bytes": step_bytes,
                          "gbs": round(step_bytes / (ms_per_step * 1e-3) / 1e9, 1),
@@ -642,6 +673,7 @@ def run_ours(args):
             "kernels": kernels,
             "roofline": roofline,
             "f32_encoder": f32_line,
+            "accumulator_modes": modes,
             "atomic_roofline": atomic_roofline,
             "cpu_baseline": cpu,
             "e2e": e2e,

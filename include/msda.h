@@ -79,7 +79,8 @@ typedef enum {
  *   adds per head), and 5.5e-2 when every point of 5,000 queries falls in one
  *   4x4 patch per level: NATIVE misses 2e-2 on contended maps. fp16 keeps 3
  *   more mantissa bits (decoder 4.1e-4). FP32_BUFFER stays at the 16-bit
- *   rounding of the result (1.7e-3 bf16) on every one of them.
+ *   rounding of the result (1.7e-3 bf16) on every one of them, and
+ *   FP16_BUFFER (below) within 2e-2 on each at close to NATIVE's speed.
  * FP32_BUFFER: atomic adds into a caller-provided fp32 workspace, then one
  *   rounding pass into grad_value. For MSDA_F32 and MSDA_F64 both modes are
  *   the same (atomics of that type into grad_value) and no workspace is needed.
@@ -106,6 +107,14 @@ typedef enum {
  * Sums far below the bound (2^-25 of it and less) fall into fp16's subnormals
  * and keep fewer bits. The adds move 64 bytes per corner and head,
  * as native accumulation does (half the fp32 buffer's).
+ * Measured (relative L2 against an fp64 reference, GB300): grad_value 1.7e-3
+ * on the decoder shape, 3.1e-3 on the Deformable-DETR encoder, 2.3e-3 on the
+ * Mask2Former encoder, 7.8e-3 with 5,000 queries in one 4x4 patch per level
+ * (NATIVE 5.5e-2); the encoder backward takes 306 us against 278 us NATIVE and
+ * 382 us with FP32_BUFFER. Limit: a 16-bit running sum stagnates once it is
+ * 2^11 times its addends, so thousands of same-sign adds into one element
+ * (all-positive grad_out with every query on one small patch) lose most of
+ * their sum; FP32_BUFFER is the mode for such inputs.
  * Workspace: B*S*M*D*2 + 20480 bytes (msda_backward_workspace_bytes). For
  * fp16, fp32 and fp64 data it is the same as MSDA_ACC_NATIVE. */
 /* MSDA_ACC_AUTO (16-bit data): NATIVE or FP32_BUFFER, chosen on the host from

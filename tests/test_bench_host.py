@@ -68,6 +68,8 @@ def test_accumulator_names():
     assert d("bf16", "fp16_buffer") == "f16" and d("bf16", "native") == "bf16"
     assert set(bench.ACCUM_MODES) == {"fp32_buffer", "native", "auto", "fp16_buffer"}
     assert bench.parse_args(["--accum", "fp16_buffer"]).accum == "fp16_buffer"
+    assert bench.parse_args(["--no-accum-lines"]).no_accum_lines
+    assert set(bench.LAUNCHES_PER_STEP) == {"fp32_buffer", "native", "fp16_buffer", "f32"}
 
 
 def test_traffic_figure_needs_matching_kernel_sources(tmp_path):

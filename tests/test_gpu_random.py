@@ -45,8 +45,12 @@ def draw(seed):
                     M=int(rng.integers(1, 10)), D=int(rng.choice(CHANNELS[dtype])), K=K,
                     levels=levels, dtype=dtype,
                     sigma_px=float(rng.choice([0.3, 1.0, 2.0, 6.0, 20.0])), seed=seed)
-    # native 16-bit adds round at every add; the fp32 buffer is the mode at parity
-    accum = binding.MSDA_ACC_FP32_BUFFER
+    # native 16-bit adds round at every add; the fp32 buffer is the mode at
+    # parity, and the scaled fp16 buffer (native adds for fp16 data) is held to
+    # the same tolerance. Drawn from a stream of its own, so that the shapes of
+    # each seed stay as they were.
+    accum = (binding.MSDA_ACC_FP32_BUFFER, binding.MSDA_ACC_FP16_BUFFER)[
+        np.random.default_rng(5000 + seed).integers(2)]
     # the fused softmax keeps a query-head's L*K weights in 16 slots per 16-byte lane
     lanes16 = w.D * (4 if dtype == "f32" else 2) // 16
     softmax = bool(rng.integers(2)) and L * K <= 16 * lanes16
@@ -103,7 +107,7 @@ def run_case(seed):
         ref = [oracle.forward(p["value"], p["shapes"], p["starts"], p["loc"], p["attn"]),
                *oracle.backward(p["value"], p["shapes"], p["starts"], p["loc"], p["attn"],
                                 p["grad_out"])]
-    label = (w.name, w.dtype, w.B, w.Q, w.M, w.D, w.K, w.levels, w.sigma_px, softmax, split)
+    label = (w.name, w.dtype, w.B, w.Q, w.M, w.D, w.K, w.levels, w.sigma_px, softmax, split, accum)
     if w.dtype == "f32":
         scale = max(float(np.max(np.abs(ref[0]))), 1e-300)
         assert np.max(np.abs(got[0] - ref[0])) / scale <= 1e-5, label
