@@ -129,3 +129,59 @@ def test_cuda_graph_with_auto_accumulation():
     assert torch.equal(outs[0], eager[0]) and torch.equal(outs[2], eager[2])
     assert torch.equal(outs[3], eager[3])
     assert _close(outs[1], eager[1])
+
+
+def test_cuda_graph_with_fp16_buffer_rescales_every_replay():
+    """MSDA_ACC_FP16_BUFFER derives its scale on the device from the
+    current grad_out and attention weights, so a captured call must follow
+    new inputs: grad_out 1000 times larger copied into the captured buffer
+    gives a grad_value 1000 times larger, not an overflowed one."""
+    t = _inputs(wl.encoder("bf16"))
+    buf = binding.BackwardBuffers(t["value"], t["loc"], t["attn"], binding.MSDA_ACC_FP16_BUFFER)
+    assert buf.workspace is not None
+    eager = [x.clone() for x in _run(t, buf=buf)]
+    torch.cuda.synchronize()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        _run(t, stream=s, buf=buf)
+    torch.cuda.current_stream().wait_stream(s)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        outs = _run(t, stream=torch.cuda.current_stream(), buf=buf)
+    for _ in range(3):
+        buf.grad_value.fill_(7.0)
+        g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(outs[2], eager[2]) and torch.equal(outs[3], eager[3])
+    assert _close(outs[1], eager[1], tol=1e-2)      # the adds' order varies between runs
+    t["grad_out"].mul_(1000.0)                       # exact in bf16 up to rounding of x1000
+    fresh_buf = binding.BackwardBuffers(t["value"], t["loc"], t["attn"],
+                                        binding.MSDA_ACC_FP16_BUFFER)
+    fresh = _run(t, buf=fresh_buf)
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.isfinite(outs[1].float()).all()
+    assert _close(outs[1], fresh[1], tol=1e-2)
+    assert _close(outs[1], eager[1].double() * 1000.0, tol=2e-2)
+
+
+def test_fp16_buffer_on_two_streams():
+    """Two problems with their own fp16 workspaces on two streams at once."""
+    a, b = _inputs(wl.encoder("bf16")), _inputs(wl.sweep(5000, 4, 4, contention=True))
+    bufs = [binding.BackwardBuffers(x["value"], x["loc"], x["attn"], binding.MSDA_ACC_FP16_BUFFER)
+            for x in (a, b)]
+    ra, rb = [x.clone() for x in _run(a, buf=bufs[0])], [x.clone() for x in _run(b, buf=bufs[1])]
+    torch.cuda.synchronize()
+    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+    bufs2 = [binding.BackwardBuffers(x["value"], x["loc"], x["attn"], binding.MSDA_ACC_FP16_BUFFER)
+             for x in (a, b)]
+    with torch.cuda.stream(s1):
+        ga = _run(a, stream=s1, buf=bufs2[0])
+    with torch.cuda.stream(s2):
+        gb = _run(b, stream=s2, buf=bufs2[1])
+    torch.cuda.synchronize()
+    for got, ref in ((ga, ra), (gb, rb)):
+        assert torch.equal(got[0], ref[0]) and torch.equal(got[2], ref[2])
+        assert torch.equal(got[3], ref[3])
+        assert _close(got[1], ref[1], tol=1e-2)
