@@ -41,6 +41,18 @@
 
 namespace msda {
 
+// w * (x[i], x[i+1]) for i = 0, 2, ..., 2N-2 in packed fp32 pairs (one
+// mul.rn.f32x2 per pair; products rounded as the scalar multiplies are).
+template <int N> __device__ __forceinline__ void scale_pairs(float *t, float w, const float *x) {
+    const float2 w2 = make_float2(w, w);
+#pragma unroll
+    for (int i = 0; i < N; ++i) {
+        const float2 y = __fmul2_rn(w2, make_float2(x[2 * i], x[2 * i + 1]));
+        t[2 * i] = y.x;
+        t[2 * i + 1] = y.y;
+    }
+}
+
 __device__ __forceinline__ void red_add_v4_f32(float *p, float a, float b, float c, float d) {
     asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(a), "f"(b),
                  "f"(c), "f"(d)
@@ -73,15 +85,19 @@ template <int LPG> struct Scatter<float, true, LPG> {
     using Acc = float;
     static constexpr int NSC = 4;
     static __device__ __forceinline__ void add(float *row, float w, const float *sc, int r) {
-        red_add_v4_f32(row + 4 * r, w * sc[0], w * sc[1], w * sc[2], w * sc[3]);
+        float t[4];
+        scale_pairs<2>(t, w, sc);
+        red_add_v4_f32(row + 4 * r, t[0], t[1], t[2], t[3]);
     }
 };
 template <typename T, int LPG> struct Scatter<T, true, LPG> {
     using Acc = float;
     static constexpr int NSC = 8;
     static __device__ __forceinline__ void add(float *row, float w, const float *sc, int r) {
-        red_add_v4_f32(row + 4 * r, w * sc[0], w * sc[1], w * sc[2], w * sc[3]);
-        red_add_v4_f32(row + 4 * LPG + 4 * r, w * sc[4], w * sc[5], w * sc[6], w * sc[7]);
+        float t[8];
+        scale_pairs<4>(t, w, sc);
+        red_add_v4_f32(row + 4 * r, t[0], t[1], t[2], t[3]);
+        red_add_v4_f32(row + 4 * LPG + 4 * r, t[4], t[5], t[6], t[7]);
     }
 };
 template <int LPG> struct Scatter<__nv_bfloat16, false, LPG> {
@@ -89,8 +105,7 @@ template <int LPG> struct Scatter<__nv_bfloat16, false, LPG> {
     static constexpr int NSC = 8;
     static __device__ __forceinline__ void add(__nv_bfloat16 *row, float w, const float *sc, int r) {
         float t[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) t[i] = w * sc[i];
+        scale_pairs<4>(t, w, sc);
         red_add_v4_bf16x2(row + 8 * r, pack16<__nv_bfloat16>(t));
     }
 };
@@ -99,8 +114,7 @@ template <int LPG> struct Scatter<__half, false, LPG> {
     static constexpr int NSC = 8;
     static __device__ __forceinline__ void add(__half *row, float w, const float *sc, int r) {
         float t[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) t[i] = w * sc[i];
+        scale_pairs<4>(t, w, sc);
         red_add_v4_f16x2(row + 8 * r, pack16<__half>(t));
     }
 };
@@ -113,8 +127,7 @@ template <int LPG> struct ScatterF16 {
     static constexpr int NSC = 8;
     static __device__ __forceinline__ void add(__half *row, float w, const float *sc, int r) {
         float t[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) t[i] = w * sc[i];
+        scale_pairs<4>(t, w, sc);
         red_add_v4_f16x2(row + 8 * r, pack16<__half>(t));
     }
 };
@@ -473,10 +486,19 @@ msda_backward_kernel(const Params p) {
                 for (int c = 0; c < 4; ++c) {
                     float x[VEC];
                     unpack_n<T, VEC>(x, v[u][c]);
-                    float acc = 0.0f;
+                    if constexpr (NARROW) {
+                        float acc = 0.0f;
 #pragma unroll
-                    for (int i = 0; i < VEC; ++i) acc = fmaf(go[i], x[i], acc);
-                    d[c] = acc;
+                        for (int i = 0; i < VEC; ++i) acc = fmaf(go[i], x[i], acc);
+                        d[c] = acc;
+                    } else {   // packed fp32 pairs: even and odd channels summed apart
+                        float2 acc = make_float2(0.0f, 0.0f);
+#pragma unroll
+                        for (int i = 0; i < VEC; i += 2)
+                            acc = __ffma2_rn(make_float2(go[i], go[i + 1]),
+                                             make_float2(x[i], x[i + 1]), acc);
+                        d[c] = acc.x + acc.y;
+                    }
                 }
                 const float wc[4] = {w[u].x, w[u].y, w[u].z, w[u].w};
                 const int oc[4] = {o[u].x, o[u].y, o[u].z, o[u].w};
