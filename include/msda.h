@@ -110,8 +110,8 @@ typedef enum {
  * Measured (relative L2 against an fp64 reference, GB300): grad_value 1.7e-3
  * on the decoder shape, 3.1e-3 on the Deformable-DETR encoder, 2.3e-3 on the
  * Mask2Former encoder, 7.8e-3 with 5,000 queries in one 4x4 patch per level
- * (NATIVE 5.5e-2); the encoder backward takes 306 us against 278 us NATIVE and
- * 382 us with FP32_BUFFER. Limit: a 16-bit running sum stagnates once it is
+ * (NATIVE 5.5e-2); the encoder backward takes 306 us against 277 us NATIVE and
+ * 383 us with FP32_BUFFER. Limit: a 16-bit running sum stagnates once it is
  * 2^11 times its addends, so thousands of same-sign adds into one element
  * (all-positive grad_out with every query on one small patch) lose most of
  * their sum; FP32_BUFFER is the mode for such inputs.
