@@ -156,3 +156,33 @@ def test_fp16_buffer_is_native_for_other_dtypes():
                               p["grad_out"])
         for x, r in zip((gv, gl, ga), ref):
             assert _rel(x.double().cpu().numpy(), r) <= tol
+
+
+def test_fp16_buffer_zero_gradient_and_empty_queries():
+    """All-zero grad_out (a zero bound: k = 0) gives exact zeros, and Q = 0
+    zeroes grad_value without touching the workspace's scale path."""
+    w = wl.decoder("bf16")
+    p = wl.make_inputs(w)
+    t = {k: _up(p[k], "bf16") for k in ("value", "loc", "attn")}
+    shapes, starts = torch.tensor(p["shapes"]).cuda(), torch.tensor(p["starts"]).cuda()
+    g = torch.zeros((w.B, w.Q, w.M * w.D), dtype=torch.bfloat16, device="cuda")
+    gv, gl, ga = binding.msda_backward(t["value"], shapes, starts, t["loc"], t["attn"], g,
+                                       accum=F16BUF)
+    torch.cuda.synchronize()
+    assert not gv.any() and not gl.any() and not ga.any()
+    loc0, attn0 = t["loc"][:, :0].contiguous(), t["attn"][:, :0].contiguous()
+    g0 = g[:, :0].contiguous()
+    gv0 = torch.full_like(t["value"], float("nan"))
+    binding.msda_backward(t["value"], shapes, starts, loc0, attn0, g0, accum=F16BUF,
+                          grad_value=gv0, grad_sampling_locations=torch.empty_like(loc0),
+                          grad_attention_weights=torch.empty_like(attn0))
+    torch.cuda.synchronize()
+    assert not gv0.any()
+
+
+@pytest.mark.parametrize("g_scale", [1e-36, 1e30])
+def test_fp16_buffer_at_the_ends_of_bf16_range(g_scale):
+    """grad_out near bf16's smallest normal numbers and near 1e30: the scale
+    moves every sum into fp16's normal range and back without loss."""
+    errs = _run(wl.encoder("bf16"), g_scale=g_scale)
+    assert max(errs.values()) <= 2e-2, errs
