@@ -29,14 +29,17 @@
 
 namespace msda {
 
-template <typename T, int LPG, bool SOFTMAX, bool SPL>
+// UMAX: samples per gather step, 8 (32 loads in flight) or 4. A query-head
+// whose L*K leaves a last chunk of 1 to 4 samples (L*K = 12: chunks of 8 and
+// 4) takes 4, so that no step gathers empty slots.
+template <typename T, int LPG, bool SOFTMAX, bool SPL, int UMAX = 8>
 __global__ void __launch_bounds__(kThreads)
 msda_forward_kernel(const Params p) {
     constexpr int VEC = Vec16<T>::N;
     constexpr int GPW = 32 / LPG;            // groups per warp
     constexpr int SPW = 64;                  // descriptors per warp per chunk
     constexpr int CH = SPW / GPW;            // samples per group per chunk
-    constexpr int U = CH < 8 ? CH : 8;       // samples per gather step (8: 32 loads in flight)
+    constexpr int U = CH < UMAX ? CH : UMAX; // samples per gather step
 
     __shared__ LevelTable lt;
     __shared__ float4 s_w[kWarpsPerBlock][SPW];
@@ -163,7 +166,7 @@ msda_forward_kernel(const Params p) {
     }
 }
 
-template <typename T, bool SOFTMAX, bool SPL>
+template <typename T, bool SOFTMAX, bool SPL, int UMAX = 8>
 static cudaError_t launch_forward_t(const Params &p, int lpg, cudaStream_t stream) {
     const int gpw = 32 / lpg;
     const int64_t per_warp = gpw >> p.split_log2;     // query-heads per warp
@@ -173,12 +176,12 @@ static cudaError_t launch_forward_t(const Params &p, int lpg, cudaStream_t strea
     if (blocks > 0x7fffffff) return cudaErrorInvalidConfiguration;
     const dim3 grid((unsigned)blocks);
     switch (lpg) {
-        case 1: msda_forward_kernel<T, 1, SOFTMAX, SPL><<<grid, kThreads, 0, stream>>>(p); break;
-        case 2: msda_forward_kernel<T, 2, SOFTMAX, SPL><<<grid, kThreads, 0, stream>>>(p); break;
-        case 4: msda_forward_kernel<T, 4, SOFTMAX, SPL><<<grid, kThreads, 0, stream>>>(p); break;
-        case 8: msda_forward_kernel<T, 8, SOFTMAX, SPL><<<grid, kThreads, 0, stream>>>(p); break;
-        case 16: msda_forward_kernel<T, 16, SOFTMAX, SPL><<<grid, kThreads, 0, stream>>>(p); break;
-        case 32: msda_forward_kernel<T, 32, SOFTMAX, SPL><<<grid, kThreads, 0, stream>>>(p); break;
+        case 1: msda_forward_kernel<T, 1, SOFTMAX, SPL, UMAX><<<grid, kThreads, 0, stream>>>(p); break;
+        case 2: msda_forward_kernel<T, 2, SOFTMAX, SPL, UMAX><<<grid, kThreads, 0, stream>>>(p); break;
+        case 4: msda_forward_kernel<T, 4, SOFTMAX, SPL, UMAX><<<grid, kThreads, 0, stream>>>(p); break;
+        case 8: msda_forward_kernel<T, 8, SOFTMAX, SPL, UMAX><<<grid, kThreads, 0, stream>>>(p); break;
+        case 16: msda_forward_kernel<T, 16, SOFTMAX, SPL, UMAX><<<grid, kThreads, 0, stream>>>(p); break;
+        case 32: msda_forward_kernel<T, 32, SOFTMAX, SPL, UMAX><<<grid, kThreads, 0, stream>>>(p); break;
         default: return cudaErrorInvalidValue;
     }
     return cudaGetLastError();
@@ -191,6 +194,12 @@ static cudaError_t launch_forward_d(const Params &p0, int lpg, bool softmax, cud
     if (p.split_log2 > 0)
         return softmax ? launch_forward_t<T, true, true>(p, lpg, stream)
                        : launch_forward_t<T, false, true>(p, lpg, stream);
+    // the chunk of CH samples per group: 8 for 16-byte lanes of a 64-byte
+    // head or wider; a last chunk of 1 to 4 samples takes 4-sample steps
+    const int last = p.LK % 8;
+    if (last >= 1 && last <= 4)
+        return softmax ? launch_forward_t<T, true, false, 4>(p, lpg, stream)
+                       : launch_forward_t<T, false, false, 4>(p, lpg, stream);
     return softmax ? launch_forward_t<T, true, false>(p, lpg, stream)
                    : launch_forward_t<T, false, false>(p, lpg, stream);
 }
