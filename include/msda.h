@@ -315,10 +315,12 @@ MSDA_API msda_status_t msda_debug_corners(const int64_t *spatial_shapes,
                                  msda_dtype_t dtype, void *stream);
 
 /* Range-checked build. libmsda_checked.so is built from the same sources
- * with every global access of every kernel first checked against the extent
- * of its tensor (derived from dims): an access that would leave its tensor is
- * skipped -- a load yields zeros, a store or add does nothing -- and a
- * per-device fault word is set; nothing traps. It is a debugging stand-in for
+ * with every global access of the forward, backward and corner kernels first
+ * checked against the extent of its tensor (derived from dims): an access
+ * that would leave its tensor is skipped -- a load yields zeros, a store or
+ * add does nothing -- and a per-context fault word is set; nothing traps. The
+ * workspace passes (zero, convert, the fp16 workspace's prepare and finish)
+ * walk a flat range of the buffer they are given, bounded by their loops. It is a debugging stand-in for
  * a memory checker, much slower than libmsda.so. The normal library exports
  * the same three entry points and never sets the word.
  * msda_checked_build: 1 in libmsda_checked.so, 0 in libmsda.so.

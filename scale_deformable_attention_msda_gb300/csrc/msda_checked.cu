@@ -3,9 +3,12 @@
 // points, which then report no faults).
 //
 // compute-sanitizer is not available where this library is tested, so the
-// checked build stands in for its memcheck: every global access of every
-// kernel is checked first against the extent of the tensor it belongs to
-// (in_tensor in msda_common.cuh). An access that would leave its tensor is
+// checked build stands in for its memcheck: every global access of the
+// operator kernels (forward, backward, corners) is checked first against the
+// extent of the tensor it belongs to (in_tensor in msda_common.cuh); the
+// workspace passes (zero, convert, the fp16 workspace's prepare and finish)
+// each walk a flat range [0, n) of the buffer they are launched over, bounded
+// by their loop conditions. An access that would leave its tensor is
 // skipped and sets bit 0 of one device word per context; the host reads and
 // clears that word after a synchronisation. Nothing traps, so a fault found
 // this way leaves the context usable.

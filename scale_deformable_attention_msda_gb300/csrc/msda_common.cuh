@@ -88,7 +88,8 @@ inline int choose_split(int64_t triples, int gpw, int LK, int forced) {
 
 // ------------------------------------------------------------ checked build
 // Built with -DMSDA_CHECKED (libmsda_checked.so), every global access of the
-// kernels is first checked against the extent of the tensor it belongs to:
+// operator kernels is first checked against the extent of the tensor it
+// belongs to:
 // an access that would leave it is skipped (a load yields zeros) and bit 0 of
 // the device word p.err is set, which msda_device_check reads and clears.
 // No access is ever made outside a tensor and nothing traps. In the normal
