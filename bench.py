@@ -694,7 +694,9 @@ def run_sweep(args):
     """Median forward / backward times (L2 flushed before each timed call) over
     the ablation grid: Q in {5000, 10000, 22223}, K in {2, 4, 8}, L in 1..4 of
     the encoder levels, linear / Morton / Hilbert dispatch, and the
-    high-contention variant (every sample inside a 4x4-pixel patch per level)."""
+    high-contention variant (every sample inside a 4x4-pixel patch per level).
+    The backward is one msda_backward call into preallocated buffers (its
+    zero, accumulate and finish steps), so every accumulator runs the same way."""
     import numpy as np
     import torch
 
@@ -726,10 +728,11 @@ def run_sweep(args):
             e[0].record()
             binding.msda_forward(value, shapes, starts, loc, attn, query_order=order, out=out)
             e[1].record()
-            binding.msda_backward_zero(buf, tdt)
-            binding.msda_backward_accumulate(value, shapes, starts, loc, attn, g, buf,
-                                             query_order=order)
-            binding.msda_backward_finish(buf, tdt)
+            binding.msda_backward(value, shapes, starts, loc, attn, g, accum=accum,
+                                  query_order=order, grad_value=buf.grad_value,
+                                  grad_sampling_locations=buf.grad_sampling_locations,
+                                  grad_attention_weights=buf.grad_attention_weights,
+                                  workspace=buf.workspace)
             e[2].record()
             torch.cuda.synchronize()
             if i >= 3:
