@@ -103,7 +103,8 @@ typedef enum {
  * and point at most), so no sum exceeds max|grad_out| * Q * A, with A = 1 for
  * msda_backward_softmax (probabilities) and L * K * max|attention weight|
  * otherwise; 2^k puts that bound below 2^15 (and, for normal inputs, at or
- * above 2^11), under fp16's largest finite value, for any bound up to 2^141.
+ * above 2^11), under fp16's largest finite value, for any bound up to 2^141,
+ * and keeps every weight times 2^k finite in fp32.
  * Sums far below the bound (2^-25 of it and less) fall into fp16's subnormals
  * and keep fewer bits. The adds move 64 bytes per corner and head,
  * as native accumulation does (half the fp32 buffer's).

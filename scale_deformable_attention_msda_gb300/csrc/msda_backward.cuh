@@ -141,8 +141,11 @@ template <int LPG> struct ScatterF16 {
 // value, 65504 (and, for normal inputs, at or above 2^11), for any bound up
 // to 2^141. Inside fp16's normal range the rounding of a sum does not depend
 // on k; a sum below 2^-25 of the bound falls into fp16's subnormals and keeps
-// fewer bits. Integer arithmetic only: every
-// thread of every block evaluates it. A zero or non-finite maximum gives k = 0.
+// fewer bits. The kernel scales each corner weight first (w 2^k, then times
+// g), so k also stays below 128 - e(max w) (max w <= max|a|, or 1 for softmax
+// weights): w 2^k is finite even when tiny gradients alone would ask for a
+// larger k. Integer arithmetic only: every thread of every block evaluates
+// it. A zero or non-finite maximum gives k = 0.
 __device__ __forceinline__ int exp_above(float x) {      // x < 2^e for 0 < x < inf
     return (int)((__float_as_uint(x) >> 23) & 0xffu) - 126;
 }
@@ -155,7 +158,8 @@ __device__ __forceinline__ float f16_scale_of(float gmax, float amax, bool have_
                         (!have_amax || (amax > 0.0f && amax <= 3.4028235e38f));
     int e = exp_above(gmax) + exp_above(Q < 1 ? (int64_t)1 : Q);
     if (have_amax) e += exp_above(amax) + exp_above(LK < 1 ? (int64_t)1 : LK);
-    const int k = finite ? min(max(15 - e, -126), 126) : 0;
+    const int kw = 127 - (have_amax ? exp_above(amax) : 1);   // w 2^k < 2^127
+    const int k = finite ? min(max(min(15 - e, kw), -126), 126) : 0;
     return __uint_as_float((uint32_t)(k + 127) << 23);  // 2^k, a normal float
 }
 

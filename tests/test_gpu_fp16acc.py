@@ -43,9 +43,11 @@ def _rel(got, ref):
     return float(np.linalg.norm(got - ref) / np.linalg.norm(ref))
 
 
-def _run(w, softmax=False, g_scale=1.0, coherent=False, accum=F16BUF):
+def _run(w, softmax=False, g_scale=1.0, coherent=False, accum=F16BUF, a_scale=1.0):
     p = wl.make_inputs(w)
     g64 = (np.abs(p["grad_out"]) if coherent else p["grad_out"]) * g_scale
+    if a_scale != 1.0:                       # the oracle gets the weights the GPU gets
+        p["attn"] = _up(p["attn"] * a_scale, w.dtype).double().cpu().numpy()
     t = {k: _up(p[k], w.dtype) for k in ("value", "loc", "attn", "logits")}
     t["grad_out"] = _up(g64, w.dtype)
     shapes = torch.tensor(p["shapes"]).cuda()
@@ -185,4 +187,13 @@ def test_fp16_buffer_at_the_ends_of_bf16_range(g_scale):
     """grad_out near bf16's smallest normal numbers and near 1e30: the scale
     moves every sum into fp16's normal range and back without loss."""
     errs = _run(wl.encoder("bf16"), g_scale=g_scale)
+    assert max(errs.values()) <= 2e-2, errs
+
+
+def test_fp16_buffer_tiny_gradient_with_large_weights():
+    """grad_out ~1e-37 with attention weights ~10 on the tiny problem: the
+    bound on the sums asks for k above 126, and a weight times 2^126 would
+    overflow fp32 before the gradient scales it back; k is capped so that
+    every weight times 2^k stays finite."""
+    errs = _run(wl.tiny().with_dtype("bf16"), g_scale=1e-37, a_scale=10.0)
     assert max(errs.values()) <= 2e-2, errs
