@@ -197,3 +197,27 @@ def test_fp16_buffer_tiny_gradient_with_large_weights():
     every weight times 2^k stays finite."""
     errs = _run(wl.tiny().with_dtype("bf16"), g_scale=1e-37, a_scale=10.0)
     assert max(errs.values()) <= 2e-2, errs
+
+
+@pytest.mark.parametrize("softmax", [False, True])
+def test_fp16_buffer_through_autograd(softmax):
+    """The differentiable wrapper with accum=MSDA_ACC_FP16_BUFFER: bf16 leaf
+    tensors, loss = <out, grad_out>, and .grad against the fp64 oracle."""
+    w = wl.decoder("bf16")
+    p = wl.make_inputs(w)
+    v = _up(p["value"], "bf16").requires_grad_(True)
+    loc = _up(p["loc"], "bf16").requires_grad_(True)
+    a = _up(p["logits"] if softmax else p["attn"], "bf16").requires_grad_(True)
+    g = _up(p["grad_out"], "bf16")
+    shapes, starts = torch.tensor(p["shapes"]).cuda(), torch.tensor(p["starts"]).cuda()
+    out = binding.multi_scale_deformable_attention(v, shapes, starts, loc, a, accum=F16BUF,
+                                                   softmax=softmax)
+    (out.float() * g.float()).sum().backward()
+    torch.cuda.synchronize()
+    args = (p["value"], p["shapes"], p["starts"], p["loc"])
+    if softmax:
+        ref = oracle.backward_softmax(*args, p["logits"], p["grad_out"])
+    else:
+        ref = oracle.backward(*args, p["attn"], p["grad_out"])
+    for got, r in zip((v.grad, loc.grad, a.grad), ref):
+        assert _rel(got.double().cpu().numpy(), r) <= 2e-2
