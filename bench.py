@@ -182,6 +182,24 @@ class ClockSampler:
                 "samples": len(busy)}
 
 
+def gather_roofline(samples: int, D: int, elt: int, forward_ms: float, sm_mhz: float,
+                    n_sms: int) -> dict:
+    """The forward's own bound: L1 data-pipe wavefronts. Every sample gathers
+    4 corner vectors of D*elt bytes, each in ceil(D*elt/128) 128-byte lines
+    (rows are D*elt-aligned), one wavefront per line; the pipe retires about
+    one wavefront per cycle per SM (ncu: 80 % of its peak at 0.8 per cycle)."""
+    lines = -(-D * elt // 128)
+    wavefronts = 4 * samples * lines
+    achieved = wavefronts / (forward_ms * 1e-3) / 1e9
+    peak = n_sms * sm_mhz * 1e6 / 1e9
+    return {"kernel": "msda_forward_kernel", "bound": "l1_wavefronts",
+            "achieved": round(achieved, 1), "peak": round(peak, 1), "unit": "G wavefronts/s",
+            "frac": round(achieved / peak, 4), "wavefronts_per_launch": wavefronts,
+            "model": "one L1 data-pipe wavefront per 128-byte line of each gathered corner "
+                     "vector (4 per sample); peak one wavefront per cycle per SM x SMs x "
+                     "median SM clock under load"}
+
+
 def measured_hbm_peak():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -600,6 +618,14 @@ def run_ours(args):
                          "the fp64 oracle is measured by the GPU tests, not here; fp16_buffer's "
                          "backward is one msda_backward call (zero and finish inside it)")
     clocks = sampler.stop() if sampler else None
+    sm_mhz = (clocks or {}).get("sm_mhz") or 2070.0
+    n_sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    gather = gather_roofline(w.samples, w.D, 2 if args.dtype != "f32" else 4, mean["forward"],
+                             sm_mhz, n_sms)
+    if f32_line is not None:
+        f32_line["gather_roofline"] = gather_roofline(w.samples, w.D, 4,
+                                                      f32_line["kernels"]["forward"]["ms"],
+                                                      sm_mhz, n_sms)
 
     # ---- end to end through the public API, host buffers, copies timed.
     # Pipelined as a training input pipeline runs: step i's inputs go in on
@@ -675,6 +701,7 @@ def run_ours(args):
             "f32_encoder": f32_line,
             "accumulator_modes": modes,
             "atomic_roofline": atomic_roofline,
+            "gather_roofline": gather,
             "cpu_baseline": cpu,
             "e2e": e2e,
             "gpu_launches": launches_per_step * args.steps,

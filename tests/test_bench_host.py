@@ -72,6 +72,19 @@ def test_accumulator_names():
     assert set(bench.LAUNCHES_PER_STEP) == {"fp32_buffer", "native", "fp16_buffer", "f32"}
 
 
+def test_gather_roofline_counts_one_wavefront_per_corner_line():
+    """bf16 D=32 (64-byte head vectors) and fp32 D=32 (128 bytes) take one
+    line per corner; fp32 D=64 takes two. Encoder: 5,689,088 samples."""
+    sys.path.insert(0, ROOT)
+    import bench
+    r = bench.gather_roofline(5689088, 32, 2, 0.105, 2070.0, 152)
+    assert r["wavefronts_per_launch"] == 4 * 5689088
+    assert r["peak"] == 314.6 and abs(r["achieved"] - 4 * 5689088 / 0.105e-3 / 1e9) < 0.1
+    assert abs(r["frac"] - r["achieved"] / r["peak"]) < 1e-3
+    assert bench.gather_roofline(100, 32, 4, 1.0, 2070.0, 152)["wavefronts_per_launch"] == 400
+    assert bench.gather_roofline(100, 64, 4, 1.0, 2070.0, 152)["wavefronts_per_launch"] == 800
+
+
 def test_traffic_figure_needs_matching_kernel_sources(tmp_path):
     sys.path.insert(0, ROOT)
     import bench
