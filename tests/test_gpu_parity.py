@@ -157,6 +157,32 @@ def test_sweep_points(Q, K, L):
     run_and_check(wl.sweep(Q, K, L), FP32BUF)
 
 
+@pytest.mark.parametrize("w", list(wl.sweep_grid()), ids=lambda w: w.name)
+def test_whole_ablation_grid_both_buffers(w):
+    """Every point of the ablation grid the sweep times (Q x K x L, bf16):
+    forward and backward with the fp32 buffer and with the scaled fp16
+    buffer, against one oracle run. K = 2 and 4 with L = 1, 2 or 3 take the
+    forward's 4-sample gather steps."""
+    p = wl.make_inputs(w)
+    ref = oracle_run(p)
+    for accum, name in ((FP32BUF, "fp32 buffer"), (binding.MSDA_ACC_FP16_BUFFER, "fp16 buffer")):
+        got = gpu_run(p, w.dtype, accum)
+        check(got, ref, w.dtype, f"{w.name} {name}")
+
+
+@pytest.mark.parametrize("w", list(wl.sweep_grid()), ids=lambda w: w.name)
+def test_whole_ablation_grid_both_buffers(w):
+    """Every point of the ablation grid the sweep times (Q x K x L, bf16):
+    forward and backward with the fp32 buffer and with the scaled fp16
+    buffer, against one oracle run. K = 2 and 4 with L = 1, 2 or 3 take the
+    forward's 4-sample gather steps."""
+    p = wl.make_inputs(w)
+    ref = oracle_run(p)
+    for accum, name in ((FP32BUF, "fp32 buffer"), (binding.MSDA_ACC_FP16_BUFFER, "fp16 buffer")):
+        got = gpu_run(p, w.dtype, accum)
+        check(got, ref, w.dtype, f"{w.name} {name}")
+
+
 @pytest.mark.parametrize("w", [wl.tiny().with_dtype("f64"), wl.decoder("f64"), wl.encoder("f64")],
                          ids=lambda w: w.name)
 def test_f64(w):
