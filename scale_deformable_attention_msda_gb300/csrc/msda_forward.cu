@@ -52,7 +52,17 @@ msda_forward_kernel(const Params p) {
     const int g = lane / LPG, r = lane % LPG;
     // sl2: log2 of the groups per query-head (0 unless SPL)
     const int sl2 = SPL ? p.split_log2 : 0;
-    const int64_t t0 = ((int64_t)blockIdx.x * kWarpsPerBlock + warp) * (GPW >> sl2);
+    // Warp task gw: the warps of one block take tasks n apart (task w*n + b
+    // for warp w of block b, n = tasks / 8), so that they do not gather the
+    // same corners at the same moment; neighbouring blocks keep neighbouring
+    // tasks. A bijection of the first 8n tasks; the rest keep their index.
+    int64_t gw = (int64_t)blockIdx.x * kWarpsPerBlock + warp;
+    if (!SPL) {
+        const int64_t tasks = (p.triples + GPW - 1) / GPW;
+        const int64_t n = tasks / kWarpsPerBlock;
+        if (gw < n * kWarpsPerBlock) gw = (gw % kWarpsPerBlock) * n + gw / kWarpsPerBlock;
+    }
+    const int64_t t0 = gw * (GPW >> sl2);
     if (t0 >= p.triples) return;
 
     // this lane's group: query-head t0 + (g >> sl2), sample subset sub
