@@ -32,9 +32,21 @@ namespace msda {
 // UMAX: samples per gather step, 8 (32 loads in flight) or 4. A query-head
 // whose L*K leaves a last chunk of 1 to 4 samples (L*K = 12: chunks of 8 and
 // 4) takes 4, so that no step gathers empty slots.
+//
+// Warps per block: 2 for the ordinary launch, so that the last wave of blocks
+// ends in smaller pieces (GB300, cold, against 8-warp blocks: encoder bf16
+// 103.0 -> 101.0 us, fp32 148.1 -> 146.0 us, Mask2Former bf16 160.4 -> 148.1
+// us); the split launches of small problems keep 8 (the decoder took 15.0 us
+// with 2-warp blocks against 13.0 us). The bound of 20 resident 2-warp blocks
+// per SM (at most 51 registers) makes the compiler take 48 registers in every
+// instantiation with no spill; left free it chose 40 for some and spilled
+// (fp32 Mask2Former 221.8 us against 213.6 us).
+template <bool SPL> __host__ __device__ constexpr int fwd_warps() { return SPL ? kWarpsPerBlock : 2; }
+
 template <typename T, int LPG, bool SOFTMAX, bool SPL, int UMAX = 8>
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(fwd_warps<SPL>() * 32, SPL ? 1 : 20)
 msda_forward_kernel(const Params p) {
+    constexpr int WPB = fwd_warps<SPL>();    // warps per block
     constexpr int VEC = Vec16<T>::N;
     constexpr int GPW = 32 / LPG;            // groups per warp
     constexpr int SPW = 64;                  // descriptors per warp per chunk
@@ -42,8 +54,8 @@ msda_forward_kernel(const Params p) {
     constexpr int U = CH < UMAX ? CH : UMAX; // samples per gather step
 
     __shared__ LevelTable lt;
-    __shared__ float4 s_w[kWarpsPerBlock][SPW];
-    __shared__ int4 s_o[kWarpsPerBlock][SPW];
+    __shared__ float4 s_w[WPB][SPW];
+    __shared__ int4 s_o[WPB][SPW];
 
     load_level_table(lt, p);
     __syncthreads();
@@ -53,14 +65,14 @@ msda_forward_kernel(const Params p) {
     // sl2: log2 of the groups per query-head (0 unless SPL)
     const int sl2 = SPL ? p.split_log2 : 0;
     // Warp task gw: the warps of one block take tasks n apart (task w*n + b
-    // for warp w of block b, n = tasks / 8), so that they do not gather the
+    // for warp w of block b, n = tasks / WPB), so that they do not gather the
     // same corners at the same moment; neighbouring blocks keep neighbouring
-    // tasks. A bijection of the first 8n tasks; the rest keep their index.
-    int64_t gw = (int64_t)blockIdx.x * kWarpsPerBlock + warp;
+    // tasks. A bijection of the first WPB*n tasks; the rest keep their index.
+    int64_t gw = (int64_t)blockIdx.x * WPB + warp;
     if (!SPL) {
         const int64_t tasks = (p.triples + GPW - 1) / GPW;
-        const int64_t n = tasks / kWarpsPerBlock;
-        if (gw < n * kWarpsPerBlock) gw = (gw % kWarpsPerBlock) * n + gw / kWarpsPerBlock;
+        const int64_t n = tasks / WPB;
+        if (gw < n * WPB) gw = (gw % WPB) * n + gw / WPB;
     }
     const int64_t t0 = gw * (GPW >> sl2);
     if (t0 >= p.triples) return;
@@ -181,17 +193,18 @@ static cudaError_t launch_forward_t(const Params &p, int lpg, cudaStream_t strea
     const int gpw = 32 / lpg;
     const int64_t per_warp = gpw >> p.split_log2;     // query-heads per warp
     const int64_t warps = (p.triples + per_warp - 1) / per_warp;
-    const int64_t blocks = (warps + kWarpsPerBlock - 1) / kWarpsPerBlock;
+    constexpr int wpb = fwd_warps<SPL>();
+    const int64_t blocks = (warps + wpb - 1) / wpb;
     if (blocks == 0) return cudaSuccess;
     if (blocks > 0x7fffffff) return cudaErrorInvalidConfiguration;
     const dim3 grid((unsigned)blocks);
     switch (lpg) {
-        case 1: msda_forward_kernel<T, 1, SOFTMAX, SPL, UMAX><<<grid, kThreads, 0, stream>>>(p); break;
-        case 2: msda_forward_kernel<T, 2, SOFTMAX, SPL, UMAX><<<grid, kThreads, 0, stream>>>(p); break;
-        case 4: msda_forward_kernel<T, 4, SOFTMAX, SPL, UMAX><<<grid, kThreads, 0, stream>>>(p); break;
-        case 8: msda_forward_kernel<T, 8, SOFTMAX, SPL, UMAX><<<grid, kThreads, 0, stream>>>(p); break;
-        case 16: msda_forward_kernel<T, 16, SOFTMAX, SPL, UMAX><<<grid, kThreads, 0, stream>>>(p); break;
-        case 32: msda_forward_kernel<T, 32, SOFTMAX, SPL, UMAX><<<grid, kThreads, 0, stream>>>(p); break;
+        case 1: msda_forward_kernel<T, 1, SOFTMAX, SPL, UMAX><<<grid, wpb * 32, 0, stream>>>(p); break;
+        case 2: msda_forward_kernel<T, 2, SOFTMAX, SPL, UMAX><<<grid, wpb * 32, 0, stream>>>(p); break;
+        case 4: msda_forward_kernel<T, 4, SOFTMAX, SPL, UMAX><<<grid, wpb * 32, 0, stream>>>(p); break;
+        case 8: msda_forward_kernel<T, 8, SOFTMAX, SPL, UMAX><<<grid, wpb * 32, 0, stream>>>(p); break;
+        case 16: msda_forward_kernel<T, 16, SOFTMAX, SPL, UMAX><<<grid, wpb * 32, 0, stream>>>(p); break;
+        case 32: msda_forward_kernel<T, 32, SOFTMAX, SPL, UMAX><<<grid, wpb * 32, 0, stream>>>(p); break;
         default: return cudaErrorInvalidValue;
     }
     return cudaGetLastError();
