@@ -163,7 +163,16 @@ __device__ __forceinline__ float f16_scale_of(float gmax, float amax, bool have_
     return __uint_as_float((uint32_t)(k + 127) << 23);  // 2^k, a normal float
 }
 
-__device__ __forceinline__ void f16_warp_store(float m, float ma, float *s) {
+// Each warp's maximum over the prepare pass's block maxima (at most
+// 2 * kF16MaxBlocks values, read in flight with the level table's) into s[warp]
+// (of |grad_out|) and s[WPB + warp] (of |attention weight|), WPB warps a block.
+template <int WPB> __device__ __forceinline__ void f16_warp_maxima(const Params &p, float *s) {
+    const int n = p.f16_nmax, total = p.f16_amax ? 2 * n : n;
+    float m = 0.0f, ma = 0.0f;
+    for (int j = threadIdx.x; j < total; j += WPB * 32) {
+        const float v = p.f16_max[j];
+        if (j < n) m = fmaxf(m, v); else ma = fmaxf(ma, v);
+    }
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) {
         m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
@@ -171,33 +180,18 @@ __device__ __forceinline__ void f16_warp_store(float m, float ma, float *s) {
     }
     if ((threadIdx.x & 31) == 0) {
         s[threadIdx.x >> 5] = m;
-        s[kWarpsPerBlock + (threadIdx.x >> 5)] = ma;
+        s[WPB + (threadIdx.x >> 5)] = ma;
     }
-}
-
-// Each warp's maximum over the prepare pass's block maxima into s[warp] (of
-// |grad_out|) and s[kWarpsPerBlock + warp] (of |attention weight|). The
-// 2 * f16_nmax <= 2 * kF16MaxBlocks values take at most two loads per thread,
-// both in flight with the level table's.
-static_assert(2 * kF16MaxBlocks <= 2 * kThreads, "two loads per thread");
-__device__ __forceinline__ void f16_warp_maxima(const Params &p, float *s) {
-    const int n = p.f16_nmax, total = p.f16_amax ? 2 * n : n;
-    const int j0 = threadIdx.x, j1 = threadIdx.x + kThreads;
-    const float v0 = j0 < total ? p.f16_max[j0] : 0.0f;
-    const float v1 = j1 < total ? p.f16_max[j1] : 0.0f;
-    const float m = fmaxf(j0 < n ? v0 : 0.0f, j1 < n ? v1 : 0.0f);
-    const float ma = fmaxf(j0 >= n ? v0 : 0.0f, j1 >= n ? v1 : 0.0f);
-    f16_warp_store(m, ma, s);
 }
 
 // After a __syncthreads that follows f16_warp_maxima: the call's 2^k; block 0
 // stores (2^k, 2^-k) for the finish pass.
-__device__ __forceinline__ float f16_block_scale(const Params &p, const float *s) {
+template <int WPB> __device__ __forceinline__ float f16_block_scale(const Params &p, const float *s) {
     float m = 0.0f, ma = 0.0f;
 #pragma unroll
-    for (int w = 0; w < kWarpsPerBlock; ++w) {
+    for (int w = 0; w < WPB; ++w) {
         m = fmaxf(m, s[w]);
-        ma = fmaxf(ma, s[kWarpsPerBlock + w]);
+        ma = fmaxf(ma, s[WPB + w]);
     }
     const float scale = f16_scale_of(m, ma, p.f16_amax != 0, p.Q, p.LK);
     if (blockIdx.x == 0 && threadIdx.x == 0) {
@@ -323,9 +317,23 @@ __device__ __forceinline__ void merge_shared_rows(float4 &w, const int4 &o, int 
 // contribution multiplied by 2^k (f16_scale_of; each block derives it from the
 // prepare pass's block maxima while it loads the level table): fp16 keeps 11
 // bits where bf16 keeps 8, at the same 64 bytes per add.
+//
+// Warps per block: 2 for the 16-byte-lane kernels of ordinary launches, so
+// that the last wave ends in smaller pieces at the same 32 resident warps per
+// SM (GB300, cold, against 8-warp blocks: Mask2Former native 390.8 -> 378.5
+// us, fp16 workspace 430.7 -> 421.5 us, encoder native 287.4 -> 283.3 us,
+// the 4x4 contention sweep native 113.8 -> 105.6 us); the narrow
+// fp32-workspace kernel (404.1 -> 408.2 us with 2) and the split launches
+// keep 8.
+template <bool NARROW, bool SPL> __host__ __device__ constexpr int bwd_warps() {
+    return (NARROW || SPL) ? kWarpsPerBlock : 2;
+}
+
 template <typename T, int LPG, bool F32ACC, bool SOFTMAX, bool NARROW, bool SPL, bool F16ACC = false>
-__global__ void __launch_bounds__(kThreads, 4)
+__global__ void __launch_bounds__(bwd_warps<NARROW, SPL>() * 32,
+                                  bwd_warps<NARROW, SPL>() == 2 ? 16 : 4)
 msda_backward_kernel(const Params p) {
+    constexpr int WPB = bwd_warps<NARROW, SPL>();   // warps per block
     static_assert(!NARROW || (F32ACC && sizeof(T) == 2), "narrow lanes: 16-bit data, fp32 workspace");
     static_assert(!F16ACC || (!F32ACC && !NARROW && sizeof(T) == 2), "fp16 workspace: 16-bit data");
     constexpr int LB = NARROW ? 8 : 16;      // bytes of one corner vector per lane
@@ -341,24 +349,24 @@ msda_backward_kernel(const Params p) {
     constexpr int NSC = NARROW ? VEC : S::NSC;
 
     __shared__ LevelTable lt;
-    __shared__ float4 s_w[kWarpsPerBlock][SPW];
-    __shared__ int4 s_o[kWarpsPerBlock][SPW];
-    __shared__ float4 s_dot[kWarpsPerBlock][SPW];
-    __shared__ float s_ga[kWarpsPerBlock][SOFTMAX ? kSoftmaxSlots : 1];
-    __shared__ float s_f16max[F16ACC ? 2 * kWarpsPerBlock : 1];
+    __shared__ float4 s_w[WPB][SPW];
+    __shared__ int4 s_o[WPB][SPW];
+    __shared__ float4 s_dot[WPB][SPW];
+    __shared__ float s_ga[WPB][SOFTMAX ? kSoftmaxSlots : 1];
+    __shared__ float s_f16max[F16ACC ? 2 * WPB : 1];
     constexpr int SLOTS = SOFTMAX ? kSoftmaxSlots / GPW : 1;   // samples per query-head
 
     load_level_table(lt, p);
-    if constexpr (F16ACC) f16_warp_maxima(p, s_f16max);
+    if constexpr (F16ACC) f16_warp_maxima<WPB>(p, s_f16max);
     __syncthreads();
     // fp16 workspace: the call's scale, folded into each corner's weight
-    const float acc_scale = F16ACC ? f16_block_scale(p, s_f16max) : 1.0f;
+    const float acc_scale = F16ACC ? f16_block_scale<WPB>(p, s_f16max) : 1.0f;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g = lane / LPG, r = lane % LPG;
     // sl2: log2 of the groups per query-head (0 unless SPL)
     const int sl2 = SPL ? p.split_log2 : 0;
-    const int64_t t0 = ((int64_t)blockIdx.x * kWarpsPerBlock + warp) * (GPW >> sl2);
+    const int64_t t0 = ((int64_t)blockIdx.x * WPB + warp) * (GPW >> sl2);
     if (t0 >= p.triples) return;
 
     const int64_t t = t0 + (g >> sl2);
@@ -586,11 +594,16 @@ static cudaError_t launch_backward_t(const Params &p, int lpg, cudaStream_t stre
     const int lanes = narrow ? 2 * lpg : lpg;
     const int64_t per_warp = (32 / lanes) >> p.split_log2;    // query-heads per warp
     const int64_t warps = (p.triples + per_warp - 1) / per_warp;
-    const int64_t blocks = (warps + kWarpsPerBlock - 1) / kWarpsPerBlock;
-    if (blocks == 0) return cudaSuccess;
-    if (blocks > 0x7fffffff) return cudaErrorInvalidConfiguration;
-    const dim3 grid((unsigned)blocks);
-#define MSDA_BWD(N, NAR) msda_backward_kernel<T, N, F32ACC, SOFTMAX, NAR, SPL, F16ACC><<<grid, kThreads, 0, stream>>>(p)
+    if (warps == 0) return cudaSuccess;
+    // blocks of bwd_warps<NAR, SPL>() warps
+#define MSDA_BWD(N, NAR)                                                                          \
+    do {                                                                                          \
+        constexpr int wpb = bwd_warps<NAR, SPL>();                                                \
+        const int64_t blocks = (warps + wpb - 1) / wpb;                                           \
+        if (blocks > 0x7fffffff) return cudaErrorInvalidConfiguration;                           \
+        msda_backward_kernel<T, N, F32ACC, SOFTMAX, NAR, SPL, F16ACC>                             \
+            <<<dim3((unsigned)blocks), wpb * 32, 0, stream>>>(p);                                 \
+    } while (0)
     if constexpr (kNarrowable) {
         if (narrow) {
             switch (lanes) {
