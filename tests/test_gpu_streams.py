@@ -185,3 +185,47 @@ def test_fp16_buffer_on_two_streams():
         assert torch.equal(got[0], ref[0]) and torch.equal(got[2], ref[2])
         assert torch.equal(got[3], ref[3])
         assert _close(got[1], ref[1], tol=1e-2)
+
+
+def test_calls_from_two_host_threads():
+    """Two host threads, each with its own stream and buffers, issue forward
+    and backward calls at the same time (ctypes releases the GIL during the
+    calls); every result matches the same calls made from one thread. The
+    range-checked library runs the same way, so its per-context fault-word
+    lookup is taken from both threads at once."""
+    import threading
+
+    from scale_deformable_attention_msda_gb300 import build
+    problems = [_inputs(wl.decoder("bf16")), _inputs(wl.sweep(5000, 4, 4))]
+    refs = [[x.clone() for x in _run(t)] for t in problems]
+    torch.cuda.synchronize()
+    for lib in (build.LIBRARY, build.CHECKED_LIBRARY):
+        binding.use_library(lib)
+        try:
+            results, errors = [None, None], []
+
+            def work(i):
+                try:
+                    s = torch.cuda.Stream()
+                    with torch.cuda.stream(s):
+                        for _ in range(10):
+                            got = _run(problems[i], stream=s)
+                    s.synchronize()
+                    results[i] = got
+                except Exception as e:                # reported on the main thread
+                    errors.append(e)
+
+            threads = [threading.Thread(target=work, args=(i,)) for i in range(2)]
+            for th in threads:
+                th.start()
+            for th in threads:
+                th.join()
+            assert not errors, errors
+            torch.cuda.synchronize()
+            assert binding.msda_device_check() == 0
+            for got, ref in zip(results, refs):
+                assert torch.equal(got[0], ref[0]) and torch.equal(got[2], ref[2])
+                assert torch.equal(got[3], ref[3])
+                assert _close(got[1], ref[1])
+        finally:
+            binding.use_library(build.LIBRARY)
