@@ -157,17 +157,21 @@ def test_sweep_points(Q, K, L):
     run_and_check(wl.sweep(Q, K, L), FP32BUF)
 
 
-@pytest.mark.parametrize("w", list(wl.sweep_grid()), ids=lambda w: w.name)
-def test_whole_ablation_grid_both_buffers(w):
-    """Every point of the ablation grid the sweep times (Q x K x L, bf16):
-    forward and backward with the fp32 buffer and with the scaled fp16
-    buffer, against one oracle run. K = 2 and 4 with L = 1, 2 or 3 take the
-    forward's 4-sample gather steps."""
+@pytest.mark.parametrize("dtype", ["f32", "bf16", "f16"])
+def test_shape_example_of_the_pages(dtype):
+    """The operand shapes the deformops README prints for its backend example:
+    value (1, 80, 4, 8) over levels (8, 8) and (4, 4), starts [0, 64]; here
+    with 10 queries and 4 points. D = 8 gives one or two lanes per
+    query-head. Plain and softmax variants; for 16-bit data both buffers."""
+    w = wl.Workload("readme_example", B=1, Q=10, M=4, D=8, K=4, levels=((8, 8), (4, 4)),
+                    dtype=dtype, sigma_px=1.5, ref="uniform", seed=4242)
     p = wl.make_inputs(w)
+    assert list(p["starts"]) == [0, 64] and p["value"].shape == (1, 80, 4, 8)
     ref = oracle_run(p)
-    for accum, name in ((FP32BUF, "fp32 buffer"), (binding.MSDA_ACC_FP16_BUFFER, "fp16 buffer")):
-        got = gpu_run(p, w.dtype, accum)
-        check(got, ref, w.dtype, f"{w.name} {name}")
+    accs = [FP32BUF] if dtype == "f32" else [FP32BUF, binding.MSDA_ACC_FP16_BUFFER]
+    for accum in accs:
+        check(gpu_run(p, dtype, accum), ref, dtype, f"example {dtype} accum {accum}")
+    _softmax_check(w, FP32BUF, f"example softmax {dtype}")
 
 
 @pytest.mark.parametrize("w", list(wl.sweep_grid()), ids=lambda w: w.name)
