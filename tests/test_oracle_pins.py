@@ -12,7 +12,9 @@
 * central finite differences of the forward for every gradient;
 * the identities that hold because out is linear in value and in attn;
 * mutation checks: plausible mistakes planted in a COPY of the oracle's C
-  source (never in the oracle itself) must each fail one of these pins.
+  source, or of the Python source of its softmax variant (never in the
+  oracle itself), must each fail one of these pins; an unmutated copy taken
+  the same way passes them all (the control).
 """
 import os
 import subprocess
@@ -439,6 +441,21 @@ def _run_checks_in_child(lib_path):
     return [x for x in line[len("FAILED:"):].split(",") if x]
 
 
+def test_pins_pass_on_an_unmutated_copy(oracle_mod):
+    """Control for the mutation checks: the oracle's C source compiled and
+    checked through the same child-process path, unchanged, fails no pin and
+    does not crash (so a caught mutant is caught by its mistake)."""
+    with open(oracle_mod.SOURCE) as f:
+        src = f.read()
+    with tempfile.TemporaryDirectory() as d:
+        path = os.path.join(d, "copy.c")
+        with open(path, "w") as f:
+            f.write(src)
+        lib = oracle_mod.compile_library(path, os.path.join(d, "c.so"))
+        failed = _run_checks_in_child(lib)
+    assert failed == [], failed
+
+
 @pytest.mark.parametrize("name", sorted(MUTATIONS))
 def test_pins_catch_planted_mistake(oracle_mod, name):
     old, new = MUTATIONS[name]
@@ -511,3 +528,57 @@ def test_softmax_variant_finite_differences(oracle_mod):
                                                    zm.reshape(logits.shape)))
         fd[i] = (fp - fm) / (2 * h)
     assert np.linalg.norm(fd - gz.reshape(-1)) <= 1e-6 * np.linalg.norm(fd)
+
+
+SOFTMAX_MUTATIONS = {
+    "softmax_over_points_only": ("    lead = z.shape[:-2]\n", "    lead = z.shape[:-1]\n"),
+    "logit_grad_drops_the_mean": ("    gz = af * (gf - np.sum(af * gf, axis=-1, keepdims=True))",
+                                  "    gz = af * gf"),
+    "logit_grad_sign": ("    gz = af * (gf - np.sum(af * gf, axis=-1, keepdims=True))",
+                        "    gz = af * (np.sum(af * gf, axis=-1, keepdims=True) - gf)"),
+    "logit_grad_wrong_axis": ("    gz = af * (gf - np.sum(af * gf, axis=-1, keepdims=True))",
+                              "    gz = af * (gf - np.sum(af * gf, axis=0, keepdims=True))"),
+}
+SOFTMAX_PINS = (test_softmax_variant_constant_map, test_softmax_variant_matches_torch_autograd,
+                test_softmax_variant_finite_differences)
+
+
+def _oracle_copy(old=None, new=None):
+    """A separate module made from the oracle's Python source, with `old`
+    replaced by `new` (no replacement: an exact copy), over the same
+    compiled library."""
+    import importlib.util
+    path = os.path.join(ROOT, "oracle", "__init__.py")
+    with open(path) as f:
+        src = f.read()
+    if old is not None:
+        assert src.count(old) == 1, old
+        src = src.replace(old, new)
+    spec = importlib.util.spec_from_loader("oracle_softmax_copy", loader=None)
+    mod = importlib.util.module_from_spec(spec)
+    mod.__file__ = path                             # the compiled library is found from here
+    exec(compile(src, path, "exec"), mod.__dict__)
+    return mod
+
+
+def test_softmax_pins_pass_on_an_unmutated_copy(oracle_mod):
+    """Control for the mutation checks below: the copy mechanism itself
+    leaves every softmax pin passing."""
+    copy = _oracle_copy()
+    for pin in SOFTMAX_PINS:
+        pin(copy)
+
+
+@pytest.mark.parametrize("name", sorted(SOFTMAX_MUTATIONS))
+def test_softmax_pins_catch_planted_mistake(oracle_mod, name):
+    """A plausible mistake planted in a COPY of the oracle's softmax variant
+    (its Python source, loaded as a separate module over the same compiled
+    library) must fail at least one of the softmax pins above."""
+    mutant = _oracle_copy(*SOFTMAX_MUTATIONS[name])
+    caught = []
+    for pin in SOFTMAX_PINS:
+        try:
+            pin(mutant)
+        except AssertionError:
+            caught.append(pin.__name__)
+    assert caught, f"no softmax pin caught mutation {name}"
